@@ -1,0 +1,138 @@
+/*
+ * mxfp4.h -- C ABI of the GB300 (sm_103a) MXFP4 GEMM library.
+ *
+ *   C[m,n] = quant(A) . B^T
+ *
+ * A is bf16 [m,k], quantized on the fly to MXFP4 (e2m1 values with one e8m0
+ * scale per 32 consecutive K elements); B is MXFP4 [n,k], quantized ahead of
+ * time; C is bf16 [m,n] with fp32 accumulation.
+ *
+ * The operation is the one benchmarked by the "kernelbot amd-mxfp4-mm"
+ * submission pages: the quantizer of submission 694791 ("MXFP4
+ * quantization: bf16 -> fp4(e2m1) + e8m0 block scales") and the
+ * `tl.dot_scaled(a, a_scale, "e2m1", b, b_scale, "e2m1", acc)` product of
+ * submission 752099, whose harness entry takes (A, B, B_q, B_shuffle,
+ * B_scale) and returns C.
+ *
+ * Conventions for every entry point
+ *   - Pointers named *_bf16 / a_fp4 / a_scale / b_* / c_* / workspace are
+ *     DEVICE pointers of the current CUDA device; the caller allocates and
+ *     owns them.  The library never allocates, never synchronizes (except
+ *     mxfp4_device_status) and only enqueues work on `stream`.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *   - Element strides (lda, ldc) are in elements, row-major.
+ *   - Errors: MXFP4_ERR_INVALID_ARG / MXFP4_ERR_UNSUPPORTED are returned
+ *     before anything is enqueued; MXFP4_ERR_CUDA reports a launch failure
+ *     (cudaGetLastError right after the launch); faults that happen later
+ *     surface at the caller's next synchronization, as with any CUDA call.
+ *   - All entry points are reentrant across streams; per-device state is
+ *     limited to cached kernel attributes.
+ */
+#ifndef MXFP4_H_
+#define MXFP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MXFP4_API __attribute__((visibility("default")))
+#else
+#define MXFP4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MXFP4_OK = 0,
+  MXFP4_ERR_INVALID_ARG = 1, /* null/unaligned pointer, bad size or stride */
+  MXFP4_ERR_UNSUPPORTED = 2, /* valid arguments this build does not handle */
+  MXFP4_ERR_WORKSPACE = 3,   /* workspace smaller than mxfp4_gemm_workspace_bytes */
+  MXFP4_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  MXFP4_ERR_TIMEOUT = 5      /* a kernel's bounded pipeline wait ran out */
+} mxfp4_status;
+
+/* Static, NUL-terminated name of a status code. */
+MXFP4_API const char* mxfp4_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+MXFP4_API int mxfp4_version(void);
+
+/*
+ * mxfp4_quant -- bf16 A[m,k] (row stride lda elements) -> MXFP4.
+ *   a_fp4   : u8 [m, k/2], dense; byte j of a row = code(2j) | code(2j+1) << 4
+ *             (even K index in the low nibble), code = sign bit 3 | e2m1 magnitude.
+ *   a_scale : u8 [m, k/32], dense; e8m0 byte = ub + 127.
+ * Block rule (submission 694791, "MXFP4 quantization"): per 32 consecutive
+ * elements, amax -> fp32 bits + 0x200000, & 0xFF800000 -> exponent field -
+ * 129 = ub, clamped to [-127, 127]; each element x is encoded as
+ * e2m1(x * 2^-ub), rounded to nearest even, saturating at 6.0; a negative
+ * value rounding to zero keeps its sign (nibble 0x8).  Subnormal inputs are
+ * exact; NaN/Inf inputs give unspecified codes.
+ * Preconditions: m >= 0, k > 0, k % 32 == 0, lda >= k, lda % 8 == 0, all
+ * pointers 16-byte aligned (a_scale: any alignment).  m == 0 is a no-op.
+ */
+MXFP4_API mxfp4_status mxfp4_quant(const void* a_bf16, int64_t m, int64_t k, int64_t lda, void* a_fp4, void* a_scale,
+                         void* stream);
+
+/*
+ * Size in bytes of the prepacked image of an MXFP4 B[n,k] (0 if n <= 0,
+ * k <= 0 or k % 32 != 0).
+ */
+MXFP4_API size_t mxfp4_prepacked_b_bytes(int64_t n, int64_t k);
+
+/*
+ * mxfp4_prepack_b -- one-time repack of MXFP4 B into the layout the tensor
+ * cores read: tiles of 128 rows x 256 K elements, data in the 128-byte
+ * swizzled K-major order and e8m0 scales in the 32-lane x 16-byte atoms
+ * that tcgen05.cp moves into tensor memory.  This replaces the pages'
+ * AMD-specific B_shuffle / `e8m0_shuffle` scale layout (submission 739530,
+ * `_sh_row` / `_sh_col`), which exists only for the MI355X MFMA lane order.
+ *   b_fp4   : u8 [n, k/2] as produced by mxfp4_quant (dense rows)
+ *   b_scale : u8 [n, k/32] as produced by mxfp4_quant (dense rows)
+ *   b_packed: u8 [b_packed_bytes], opaque; valid only for this (n, k).
+ * Preconditions: n > 0, k > 0, k % 32 == 0, b_packed_bytes >=
+ * mxfp4_prepacked_b_bytes(n, k), b_fp4 and b_packed 16-byte aligned.
+ */
+MXFP4_API mxfp4_status mxfp4_prepack_b(const void* b_fp4, const void* b_scale, int64_t n, int64_t k, void* b_packed,
+                             size_t b_packed_bytes, void* stream);
+
+/*
+ * Workspace bytes mxfp4_gemm needs for this shape (0 for m <= 64, where
+ * quantized A never leaves shared memory).
+ */
+MXFP4_API size_t mxfp4_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);
+
+/*
+ * mxfp4_gemm -- C[m,n] (row stride ldc) = bf16( quant(A) . B^T ), fp32
+ * accumulation; the summation order is unspecified but deterministic for a
+ * given shape and device.
+ *   a_bf16   : bf16 [m, k], row stride lda elements
+ *   b_packed : image from mxfp4_prepack_b for (n, k)
+ *   c_bf16   : bf16 [m, n], row stride ldc elements (written, not read)
+ *   workspace: device scratch of at least mxfp4_gemm_workspace_bytes(m,n,k)
+ *              bytes (may be NULL when that is 0); 16-byte aligned.
+ * m <= 64: one launch; A is quantized inside the GEMM kernel.  m > 64: a
+ * quantization launch writes A's operand image into the workspace and the
+ * GEMM launch reads it (programmatic dependent launch overlaps the two).
+ * Preconditions: m, n > 0, k > 0, k % 32 == 0, lda >= k, lda % 8 == 0,
+ * ldc >= n, ldc % 8 == 0, a_bf16 / b_packed / c_bf16 16-byte aligned.
+ */
+MXFP4_API mxfp4_status mxfp4_gemm(const void* a_bf16, int64_t m, int64_t k, int64_t lda, const void* b_packed, int64_t n,
+                        void* c_bf16, int64_t ldc, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mxfp4_device_status -- synchronize `stream`, then report and clear the
+ * device-side watchdog flag: MXFP4_ERR_TIMEOUT if any kernel of this
+ * library on the current device gave up a bounded pipeline wait since the
+ * last call, MXFP4_ERR_CUDA if the synchronization failed, else MXFP4_OK.
+ * This is a diagnostic call; it blocks the host.
+ */
+MXFP4_API mxfp4_status mxfp4_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_H_ */

@@ -1,0 +1,133 @@
+"""GB300 (sm_103a) MXFP4 GEMM:  C[m,n] = quant(A) . B^T.
+
+A is bf16 and is quantized on the fly to MXFP4 (e2m1 values, one e8m0 scale
+per 32 K elements); B is MXFP4, prepacked once into the tensor-core layout; C
+is bf16.  The computation lives in hand-written CUDA kernels behind a C ABI
+(include/mxfp4.h, built into _build/libmxfp4.so); this package is the thin
+PyTorch-facing binding: it allocates outputs with torch, passes device
+pointers and the current stream, and raises on any non-OK status.
+
+    import precision_bf16_mxfp4_gb300 as mx
+    bq, bs = mx.quant(b_bf16)                 # MXFP4 weights (linear layout)
+    packed = mx.prepack_b(bq, bs)             # one-time repack
+    c = mx.gemm(a_bf16, packed, n)            # fused quant + GEMM
+"""
+from __future__ import annotations
+
+from . import _lib
+from ._lib import (  # noqa: F401  (raw C-ABI names)
+    Mxfp4Error,
+    mxfp4_device_status,
+    mxfp4_gemm,
+    mxfp4_gemm_workspace_bytes,
+    mxfp4_prepack_b,
+    mxfp4_prepacked_b_bytes,
+    mxfp4_quant,
+    mxfp4_status_string,
+    mxfp4_version,
+)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(device):
+    torch = _torch()
+    return ctypes_void(torch.cuda.current_stream(device).cuda_stream)
+
+
+def ctypes_void(v):
+    import ctypes
+    return ctypes.c_void_p(v)
+
+
+def _check(status: int, where: str):
+    if status != _lib.MXFP4_OK:
+        raise Mxfp4Error(status, where)
+
+
+def _require_cuda(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+
+
+class PackedB:
+    """Prepacked MXFP4 weights: an opaque uint8 device buffer valid for (n, k)."""
+
+    def __init__(self, buf, n: int, k: int):
+        self.buf, self.n, self.k = buf, n, k
+
+    @property
+    def device(self):
+        return self.buf.device
+
+
+def quant(a, out_q=None, out_scale=None):
+    """bf16 [m,k] CUDA tensor -> (fp4x2 uint8 [m,k/2], e8m0 uint8 [m,k/32])."""
+    torch = _torch()
+    _require_cuda(a, "a")
+    if a.dtype != torch.bfloat16 or a.dim() != 2 or a.stride(1) != 1:
+        raise ValueError("a must be a 2-D bf16 tensor with unit column stride")
+    m, k = a.shape
+    q = out_q if out_q is not None else torch.empty((m, k // 2), dtype=torch.uint8, device=a.device)
+    s = out_scale if out_scale is not None else torch.empty((m, k // 32), dtype=torch.uint8, device=a.device)
+    st = mxfp4_quant(ctypes_void(a.data_ptr()), m, k, a.stride(0), ctypes_void(q.data_ptr()),
+                     ctypes_void(s.data_ptr()), _stream_handle(a.device))
+    _check(st, "mxfp4_quant")
+    return q, s
+
+
+def prepack_b(b_q, b_scale) -> PackedB:
+    """MXFP4 B (fp4x2 uint8 [n,k/2], e8m0 uint8 [n,k/32]) -> PackedB."""
+    torch = _torch()
+    _require_cuda(b_q, "b_q")
+    _require_cuda(b_scale, "b_scale")
+    b_q = b_q.contiguous()
+    b_scale = b_scale.contiguous()
+    n, k = b_q.shape[0], b_q.shape[1] * 2
+    if tuple(b_scale.shape) != (n, k // 32):
+        raise ValueError("b_scale must be [n, k/32]")
+    nbytes = mxfp4_prepacked_b_bytes(n, k)
+    if nbytes == 0:
+        raise ValueError("unsupported (n, k)")
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=b_q.device)
+    st = mxfp4_prepack_b(ctypes_void(b_q.data_ptr()), ctypes_void(b_scale.data_ptr()), n, k,
+                         ctypes_void(buf.data_ptr()), nbytes, _stream_handle(b_q.device))
+    _check(st, "mxfp4_prepack_b")
+    return PackedB(buf, n, k)
+
+
+def workspace_bytes(m: int, n: int, k: int) -> int:
+    return mxfp4_gemm_workspace_bytes(m, n, k)
+
+
+def gemm(a, packed: PackedB, out=None, workspace=None):
+    """C = quant(a) . B^T as bf16 [m, n]; `out` and `workspace` may be preallocated."""
+    torch = _torch()
+    _require_cuda(a, "a")
+    if a.dtype != torch.bfloat16 or a.dim() != 2 or a.stride(1) != 1:
+        raise ValueError("a must be a 2-D bf16 tensor with unit column stride")
+    m, k = a.shape
+    if k != packed.k:
+        raise ValueError("a and packed B disagree on k")
+    n = packed.n
+    c = out if out is not None else torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    need = mxfp4_gemm_workspace_bytes(m, n, k)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=a.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = mxfp4_gemm(ctypes_void(a.data_ptr()), m, k, a.stride(0), ctypes_void(packed.buf.data_ptr()), n,
+                    ctypes_void(c.data_ptr()), c.stride(0), ctypes_void(ws_ptr), ws_bytes,
+                    _stream_handle(a.device))
+    _check(st, "mxfp4_gemm")
+    return c
+
+
+def device_status(device=None):
+    """Synchronize the current stream and raise if a kernel's bounded wait ran out."""
+    torch = _torch()
+    dev = device if device is not None else torch.cuda.current_device()
+    _check(mxfp4_device_status(_stream_handle(dev)), "mxfp4_device_status")

@@ -1,0 +1,90 @@
+// C ABI of the MXFP4 library: argument validation, then kernel launches on
+// the caller's stream.  Nothing here allocates device memory or blocks,
+// except mxfp4_device_status.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/mxfp4.h"
+#include "mxfp4_device.cuh"
+#include "mxfp4_launch.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mxfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA; }
+
+bool valid_k(int64_t k) { return k > 0 && (k % 32) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mxfp4_status_string(int status) {
+  switch (status) {
+    case MXFP4_OK: return "MXFP4_OK";
+    case MXFP4_ERR_INVALID_ARG: return "MXFP4_ERR_INVALID_ARG";
+    case MXFP4_ERR_UNSUPPORTED: return "MXFP4_ERR_UNSUPPORTED";
+    case MXFP4_ERR_WORKSPACE: return "MXFP4_ERR_WORKSPACE";
+    case MXFP4_ERR_CUDA: return "MXFP4_ERR_CUDA";
+    case MXFP4_ERR_TIMEOUT: return "MXFP4_ERR_TIMEOUT";
+    default: return "MXFP4_ERR_UNKNOWN";
+  }
+}
+
+int mxfp4_version(void) { return 100; }
+
+mxfp4_status mxfp4_quant(const void* a_bf16, int64_t m, int64_t k, int64_t lda, void* a_fp4, void* a_scale,
+                         void* stream) {
+  if (m < 0 || !valid_k(k) || lda < k || (lda % 8) != 0) return MXFP4_ERR_INVALID_ARG;
+  if (m == 0) return MXFP4_OK;
+  if (!a_bf16 || !a_fp4 || !a_scale || !aligned16(a_bf16) || !aligned16(a_fp4)) return MXFP4_ERR_INVALID_ARG;
+  return from_cuda(
+      mxfp4::launch_quant_linear(a_bf16, m, k, lda, a_fp4, a_scale, static_cast<cudaStream_t>(stream)));
+}
+
+size_t mxfp4_prepacked_b_bytes(int64_t n, int64_t k) {
+  if (n <= 0 || !valid_k(k)) return 0;
+  return static_cast<size_t>(mxfp4::image_bytes(n, k));
+}
+
+mxfp4_status mxfp4_prepack_b(const void* b_fp4, const void* b_scale, int64_t n, int64_t k, void* b_packed,
+                             size_t b_packed_bytes, void* stream) {
+  if (n <= 0 || !valid_k(k)) return MXFP4_ERR_INVALID_ARG;
+  if (!b_fp4 || !b_scale || !b_packed || !aligned16(b_fp4) || !aligned16(b_packed)) return MXFP4_ERR_INVALID_ARG;
+  if (b_packed_bytes < mxfp4_prepacked_b_bytes(n, k)) return MXFP4_ERR_INVALID_ARG;
+  return from_cuda(mxfp4::launch_prepack(b_fp4, b_scale, n, k, b_packed, static_cast<cudaStream_t>(stream)));
+}
+
+size_t mxfp4_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k) {
+  mxfp4::GemmPlan plan;
+  if (m <= 0 || n <= 0 || !valid_k(k)) return 0;
+  if (mxfp4::make_gemm_plan(m, n, k, &plan) != 0) return 0;
+  return plan.workspace;
+}
+
+mxfp4_status mxfp4_gemm(const void* a_bf16, int64_t m, int64_t k, int64_t lda, const void* b_packed, int64_t n,
+                        void* c_bf16, int64_t ldc, void* workspace, size_t workspace_bytes, void* stream) {
+  if (m <= 0 || n <= 0 || !valid_k(k) || lda < k || (lda % 8) != 0 || ldc < n || (ldc % 8) != 0)
+    return MXFP4_ERR_INVALID_ARG;
+  if (!a_bf16 || !b_packed || !c_bf16 || !aligned16(a_bf16) || !aligned16(b_packed) || !aligned16(c_bf16))
+    return MXFP4_ERR_INVALID_ARG;
+  mxfp4::GemmPlan plan;
+  if (mxfp4::make_gemm_plan(m, n, k, &plan) != 0) return MXFP4_ERR_UNSUPPORTED;
+  if (plan.workspace > 0) {
+    if (!workspace || workspace_bytes < plan.workspace) return MXFP4_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MXFP4_ERR_INVALID_ARG;
+  }
+  return from_cuda(mxfp4::launch_gemm(plan, a_bf16, m, k, lda, b_packed, n, c_bf16, ldc, workspace,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+mxfp4_status mxfp4_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MXFP4_ERR_CUDA;
+  int flag = 0;
+  if (mxfp4::read_and_clear_timeout_flag(&flag) != cudaSuccess) return MXFP4_ERR_CUDA;
+  return flag ? MXFP4_ERR_TIMEOUT : MXFP4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,137 @@
+// Device-side building blocks shared by the MXFP4 kernels: the block-scale
+// rule, the e2m1 encoder, and the tiled operand image that the tcgen05 MMA
+// reads through bulk copies.
+//
+// Quantization rule (kernelbot amd-mxfp4-mm, submission 694791, "MXFP4
+// quantization: bf16 -> fp4(e2m1) + e8m0 block scales"; exponent-field form
+// as in submission 752099 `_bf16_to_fp4_hw`):
+//   amax over 32 consecutive K elements; u = (fp32 bits of amax + 0x200000)
+//   & 0xFF800000; ub = clamp(exponent field of u - 129, -127, 127);
+//   e8m0 = ub + 127; each element x -> e2m1(x * 2^-ub) rounded to nearest
+//   even on the grid {0,.5,1,1.5,2,3,4,6}, saturating at 6, sign in bit 3;
+//   two codes per byte, even K index in the low nibble.
+#pragma once
+#include <cstdint>
+
+namespace mxfp4 {
+
+// ------------------------------------------------------------ image layout
+// An MXFP4 matrix X[R, K] is stored for the MMA as tiles of 128 rows x 256 K
+// elements.  Data region: tile (rt, kt) at (rt * KT + kt) * 16384 bytes,
+// holding 128 rows of 128 bytes in the 128-byte-swizzled K-major order the
+// MMA descriptor expects (16-byte chunk c of row r sits at chunk c ^ (r & 7)).
+// Scale region (after all data): tile (rt, kt) at (rt * KT + kt) * 1024,
+// two 512-byte atoms (K blocks 0-3, 4-7); inside an atom, row r and block b
+// sit at (r % 32) * 16 + (r / 32) * 4 + b, the 32-lane x 16-byte shape that
+// tcgen05.cp copies into tensor memory.  Rows beyond R and K beyond the
+// matrix are zero in the weight image.
+constexpr int kTileRows = 128;
+constexpr int kTileK = 256;
+constexpr int kTileDataBytes = 16384;
+constexpr int kTileSfBytes = 1024;
+constexpr int kAtomBytes = 512;
+
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+__host__ __device__ inline int64_t image_bytes(int64_t rows, int64_t k) {
+  return ceil_div(rows, kTileRows) * ceil_div(k, kTileK) * (kTileDataBytes + kTileSfBytes);
+}
+__host__ __device__ inline int64_t image_sf_region(int64_t rows, int64_t k) {
+  return ceil_div(rows, kTileRows) * ceil_div(k, kTileK) * kTileDataBytes;
+}
+// byte of row r (0..127), packed-K byte kb (0..127) inside a data tile
+__host__ __device__ inline int tile_data_offset(int r, int kbyte) {
+  return r * 128 + ((((kbyte >> 4) ^ (r & 7)) & 7) << 4) + (kbyte & 15);
+}
+// scale byte of row r (0..127), K block b (0..7) inside a scale tile
+__host__ __device__ inline int tile_sf_offset(int r, int b) {
+  return ((b >> 2) * kAtomBytes) + ((r & 31) << 4) + ((r >> 5) << 2) + (b & 3);
+}
+
+// ------------------------------------------------------------ quantization
+// Largest |x| among 8 bf16 values, as a 15-bit magnitude pattern (for finite
+// values the pattern order is the magnitude order).
+__device__ __forceinline__ uint32_t absmax8_bits(const uint4& w) {
+  uint32_t a = __vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu);
+  uint32_t b = __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu);
+  uint32_t c = __vmaxu2(a, b);
+  return max(c & 0xFFFFu, c >> 16);
+}
+
+// Unbiased block exponent ub from the bf16 magnitude pattern of amax.
+__device__ __forceinline__ int block_exponent(uint32_t amax_bits) {
+  uint32_t u = ((amax_bits << 16) + 0x200000u) & 0xFF800000u;
+  int ub = (int)((u >> 23) & 0xFFu) - 129;
+  return min(max(ub, -127), 127);
+}
+
+// 2^-ub as an fp32 (ub <= 126 for any bf16 input, so this is a normal number).
+__device__ __forceinline__ float inverse_scale(int ub) {
+  return __uint_as_float((uint32_t)(127 - ub) << 23);
+}
+
+// Magnitude code of a non-negative q by comparison with the grid midpoints;
+// a midpoint goes to the neighbour whose code is even.
+__device__ __forceinline__ uint32_t e2m1_code_sw(float q) {
+  return (uint32_t)(q > 0.25f) + (uint32_t)(q >= 0.75f) + (uint32_t)(q > 1.25f) + (uint32_t)(q >= 1.75f) +
+         (uint32_t)(q > 2.5f) + (uint32_t)(q >= 3.5f) + (uint32_t)(q > 5.0f);
+}
+
+// Two values -> one byte (lo in bits 0-3, hi in bits 4-7) with the hardware
+// round-to-nearest-even, saturating e2m1 conversion.  The first source
+// operand of the conversion lands in the upper nibble.
+__device__ __forceinline__ uint32_t e2m1x2_hw(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Encode 8 consecutive bf16 values (K order: w.x low half first) with the
+// block's inverse scale into 4 bytes of packed e2m1 (byte i holds elements
+// 2i and 2i+1).  Signs come from the inputs, so values that round to zero
+// keep their sign (0x8 for negatives).
+template <bool kHardwareCvt>
+__device__ __forceinline__ uint32_t encode8(const uint4& w, float inv_scale) {
+  const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+  uint32_t out = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t v = words[i];
+    const float x0 = __uint_as_float(v << 16) * inv_scale;
+    const float x1 = __uint_as_float(v & 0xFFFF0000u) * inv_scale;
+    uint32_t byte;
+    if constexpr (kHardwareCvt) {
+      byte = e2m1x2_hw(x0, x1) & 0xFFu;
+    } else {
+      byte = e2m1_code_sw(fabsf(x0)) | (e2m1_code_sw(fabsf(x1)) << 4);
+    }
+    byte |= ((v >> 12) & 0x8u) | ((v >> 24) & 0x80u);  // input signs -> bits 3 and 7
+    out |= byte << (8 * i);
+  }
+  return out;
+}
+
+// One lane's share of a 32-element block: 8 elements (16 bytes of bf16).
+// Lanes 4j..4j+3 of a warp hold block j; the block maximum is formed with two
+// butterfly shuffles.  Returns the packed 4 bytes; `scale_byte` gets e8m0.
+template <bool kHardwareCvt>
+__device__ __forceinline__ uint32_t quantize_lane(const uint4& w, uint32_t& scale_byte) {
+  uint32_t amax = absmax8_bits(w);
+  amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+  const int ub = block_exponent(amax);
+  scale_byte = (uint32_t)(ub + 127);
+  return encode8<kHardwareCvt>(w, inverse_scale(ub));
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+}  // namespace mxfp4

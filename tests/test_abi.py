@@ -1,0 +1,118 @@
+"""CPU tests of the C-ABI library: it builds for sm_103a, loads, exports every
+symbol include/mxfp4.h declares, and rejects bad arguments before touching a
+GPU.  No compute call is made here."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import precision_bf16_mxfp4_gb300 as mx
+from precision_bf16_mxfp4_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxfp4.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxfp4_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def test_header_declares_the_documented_entry_points():
+    names = _declared_functions()
+    for required in ("mxfp4_quant", "mxfp4_prepack_b", "mxfp4_gemm", "mxfp4_prepacked_b_bytes",
+                     "mxfp4_gemm_workspace_bytes", "mxfp4_status_string", "mxfp4_device_status"):
+        assert required in names
+    assert set(names) == set(_lib.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True, check=True)
+    exported = set(re.findall(r"\bT\s+(mxfp4_\w+)", out.stdout))
+    for name in _declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_library_is_built_for_sm_103a():
+    out = subprocess.run(["cuobjdump", "--list-elf", build.LIB], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out.stdout
+
+
+def test_status_strings_and_version(lib):
+    assert mx.mxfp4_status_string(0) == "MXFP4_OK"
+    assert mx.mxfp4_status_string(5) == "MXFP4_ERR_TIMEOUT"
+    assert mx.mxfp4_status_string(99) == "MXFP4_ERR_UNKNOWN"
+    assert mx.mxfp4_version() >= 100
+
+
+def _image_bytes(rows, k):
+    return -(-rows // 128) * -(-k // 256) * (16384 + 1024)
+
+
+@pytest.mark.parametrize("n,k", [(2880, 512), (2112, 7168), (1, 32), (129, 288), (7168, 2048)])
+def test_prepacked_size(n, k):
+    assert mx.mxfp4_prepacked_b_bytes(n, k) == _image_bytes(n, k)
+
+
+def test_prepacked_size_rejects_bad_shapes():
+    assert mx.mxfp4_prepacked_b_bytes(0, 512) == 0
+    assert mx.mxfp4_prepacked_b_bytes(16, 48) == 0
+    assert mx.mxfp4_prepacked_b_bytes(16, -32) == 0
+
+
+@pytest.mark.parametrize("m,n,k", [(4, 2880, 512), (32, 4096, 512), (16, 2112, 7168), (64, 7168, 2048)])
+def test_small_m_needs_no_workspace(m, n, k):
+    assert mx.mxfp4_gemm_workspace_bytes(m, n, k) == 0
+
+
+@pytest.mark.parametrize("m,n,k", [(256, 3072, 1536), (4096, 7168, 2048), (65, 8, 32)])
+def test_large_m_workspace_is_the_activation_image(m, n, k):
+    assert mx.mxfp4_gemm_workspace_bytes(m, n, k) == _image_bytes(m, k)
+
+
+P = ctypes.c_void_p
+
+
+def test_gemm_rejects_bad_arguments_without_a_gpu():
+    fake = P(0x10000)  # aligned, never dereferenced: validation fails first
+    E = _lib.MXFP4_ERR_INVALID_ARG
+    assert mx.mxfp4_gemm(fake, 4, 48, 48, fake, 16, fake, 16, None, 0, None) == E       # k % 32
+    assert mx.mxfp4_gemm(fake, 0, 64, 64, fake, 16, fake, 16, None, 0, None) == E       # m == 0
+    assert mx.mxfp4_gemm(fake, 4, 64, 32, fake, 16, fake, 16, None, 0, None) == E       # lda < k
+    assert mx.mxfp4_gemm(fake, 4, 64, 68, fake, 16, fake, 16, None, 0, None) == E       # lda % 8
+    assert mx.mxfp4_gemm(fake, 4, 64, 64, fake, 16, fake, 12, None, 0, None) == E       # ldc < n
+    assert mx.mxfp4_gemm(None, 4, 64, 64, fake, 16, fake, 16, None, 0, None) == E       # null A
+    assert mx.mxfp4_gemm(P(0x10008), 4, 64, 64, fake, 16, fake, 16, None, 0, None) == E  # unaligned A
+    assert mx.mxfp4_gemm(fake, 256, 64, 64, fake, 16, fake, 16, None, 0, None) == _lib.MXFP4_ERR_WORKSPACE
+
+
+def test_quant_and_prepack_reject_bad_arguments_without_a_gpu():
+    fake = P(0x10000)
+    E = _lib.MXFP4_ERR_INVALID_ARG
+    assert mx.mxfp4_quant(fake, 4, 40, 40, fake, fake, None) == E
+    assert mx.mxfp4_quant(fake, -1, 64, 64, fake, fake, None) == E
+    assert mx.mxfp4_quant(fake, 0, 64, 64, fake, fake, None) == _lib.MXFP4_OK  # empty is a no-op
+    assert mx.mxfp4_prepack_b(fake, fake, 16, 64, fake, 10, None) == E          # buffer too small
+    assert mx.mxfp4_prepack_b(fake, fake, 0, 64, fake, 1 << 20, None) == E
+
+
+def test_product_path_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "precision_bf16_mxfp4_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.replace("the oracle", "").lower() or f == "inputs.py", f

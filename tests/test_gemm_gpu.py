@@ -1,0 +1,158 @@
+"""GPU parity of mxfp4_gemm against the fp64 oracle.
+
+C must satisfy |C - ref| <= 2^-7 |ref| + 1e-3 max|ref| everywhere the oracle
+is evaluated; quantized A inside the fused kernel is checked bit-exactly
+through an identity-B product, which makes C equal dequant(quant(A)).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import precision_bf16_mxfp4_gb300 as mx
+from precision_bf16_mxfp4_gb300 import inputs
+from tests.helpers import assert_close_to_ref, bf16_bits, packed_from_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(a_cpu, packed, lda=None, ldc=None, poison=True):
+    m, k = a_cpu.shape
+    n = packed.n
+    if lda is not None and lda != k:
+        big = torch.zeros((m, lda), dtype=torch.bfloat16)
+        big[:, :k] = a_cpu
+        a_dev = big.cuda()[:, :k]
+    else:
+        a_dev = a_cpu.cuda()
+    ldc = ldc or n
+    c_full = torch.full((m, ldc), float("nan") if poison else 0.0, dtype=torch.bfloat16, device="cuda")
+    c = c_full[:, :n]
+    mx.gemm(a_dev, packed, out=c)
+    mx.device_status()
+    return c.float().cpu().numpy(), c_full
+
+
+def _oracle_full(a_cpu, bq, bs):
+    aq, a_s = oracle.quant(bf16_bits(a_cpu))
+    return oracle.gemm_via_dequant(aq, a_s, bq, bs)
+
+
+SMALL_FULL = ["m4_n2880_k512", "m32_n4096_k512", "m32_n2880_k512", "m16_n2112_k7168", "m64_n7168_k2048",
+              "m256_n3072_k1536"]
+
+
+@pytest.mark.parametrize("name", SMALL_FULL)
+def test_gemm_workload_full_output(name):
+    a, b = inputs.make_inputs(name)
+    packed, bq, bs = packed_from_oracle(b)
+    got, _ = _run(a, packed)
+    ref = _oracle_full(a, bq, bs)
+    assert_close_to_ref(got, ref, what=name)
+
+
+def test_gemm_large_workload_sampled():
+    name = "m4096_n7168_k2048"
+    a, b = inputs.make_inputs(name)
+    packed, bq, bs = packed_from_oracle(b)
+    got, _ = _run(a, packed, poison=True)
+    assert np.all(np.isfinite(got))
+    aq, a_s = oracle.quant(bf16_bits(a))
+    rng = np.random.default_rng(0)
+    rows = np.concatenate([rng.integers(0, a.shape[0], 3000), np.repeat([0, 127, 128, 4095], 64)])
+    cols = np.concatenate([rng.integers(0, b.shape[0], 3000), np.tile(np.arange(0, 7168, 112), 4)])
+    ref = oracle.gemm_entries(aq, a_s, bq, bs, rows, cols)
+    # whole rows and columns through the library matmul on the dequantized values
+    full_rows = [0, 1, 129, 2047, 4095]
+    ref_rows = oracle.dequant(aq[full_rows], a_s[full_rows]) @ oracle.dequant(bq, bs).T
+    full_cols = [0, 255, 256, 7167]
+    ref_cols = oracle.dequant(aq, a_s) @ oracle.dequant(bq[full_cols], bs[full_cols]).T
+    scale = max(np.abs(ref).max(), np.abs(ref_rows).max(), np.abs(ref_cols).max())
+    assert_close_to_ref(got[rows, cols], ref, scale=scale, what="sampled")
+    assert_close_to_ref(got[full_rows], ref_rows, scale=scale, what="rows")
+    assert_close_to_ref(got[:, full_cols], ref_cols, scale=scale, what="cols")
+
+
+@pytest.mark.parametrize("m", [1, 4, 16, 17, 32, 64, 65, 200, 256])
+def test_fused_and_image_quant_bit_exact_through_identity(m):
+    """B = identity (code 1.0, scale 2^0): C[i, j] = dequant(quant(A))[i, j]
+    exactly, so every in-kernel quantized element is visible in C."""
+    k = 512
+    n = k
+    bq = np.zeros((n, k // 2), np.uint8)
+    for j in range(n):
+        bq[j, j // 2] = 0x2 if j % 2 == 0 else 0x20
+    bs = np.full((n, k // 32), 127, np.uint8)
+    packed = mx.prepack_b(torch.from_numpy(bq).cuda(), torch.from_numpy(bs).cuda())
+    a = inputs.random_bf16(m, k, seed=100 + m, std=2.0)
+    got, _ = _run(a, packed)
+    aq, a_s = oracle.quant(bf16_bits(a))
+    want = torch.from_numpy(oracle.dequant(aq, a_s)).to(torch.bfloat16).float().numpy()
+    np.testing.assert_array_equal(got, want)
+
+
+RAGGED = [(1, 1, 32), (3, 100, 96), (4, 129, 288), (16, 300, 544), (17, 128, 256), (33, 257, 160),
+          (64, 1000, 2080), (65, 131, 96), (130, 260, 544), (200, 520, 1024), (384, 384, 256)]
+
+
+@pytest.mark.parametrize("m,n,k", RAGGED)
+def test_gemm_ragged_shapes_with_padded_strides(m, n, k):
+    a = inputs.random_bf16(m, k, seed=m * 7 + n * 3 + k)
+    b = inputs.random_bf16(n, k, seed=m + n + k, std=0.5)
+    packed, bq, bs = packed_from_oracle(b)
+    lda = k + 8 * ((m % 3) + 1)
+    ldc = n + (8 - n % 8) % 8 + 8
+    got, c_full = _run(a, packed, lda=lda, ldc=ldc)
+    assert_close_to_ref(got, _oracle_full(a, bq, bs), what=f"{m}x{n}x{k}")
+    assert torch.isnan(c_full[:, n:]).all(), "wrote outside the [m, n] window"
+
+
+def test_gemm_deterministic_and_reusable_workspace():
+    for name in ("m16_n2112_k7168", "m256_n3072_k1536"):
+        a, b = inputs.make_inputs(name)
+        packed, _, _ = packed_from_oracle(b)
+        a_dev = a.cuda()
+        ws_bytes = mx.workspace_bytes(*a.shape[:1], packed.n, a.shape[1])
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda") if ws_bytes else None
+        c1 = mx.gemm(a_dev, packed, workspace=ws)
+        c2 = mx.gemm(a_dev, packed, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+
+
+def test_gemm_on_a_side_stream_matches():
+    a, b = inputs.make_inputs("m32_n2880_k512")
+    packed, bq, bs = packed_from_oracle(b)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        c = mx.gemm(a.cuda(), packed)
+    s.synchronize()
+    assert_close_to_ref(c.float().cpu().numpy(), _oracle_full(a, bq, bs))
+
+
+def test_gemm_reports_small_workspace():
+    a = inputs.random_bf16(256, 512, seed=1).cuda()
+    b = inputs.random_bf16(128, 512, seed=2)
+    packed, _, _ = packed_from_oracle(b)
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(mx.Mxfp4Error) as e:
+        mx.gemm(a, packed, workspace=ws)
+    assert e.value.status == 3
+
+
+def test_prepack_roundtrip_through_gemm_columns():
+    """Each weight row j reappears as column j of C when A = one-hot rows."""
+    n, k = 300, 544
+    b = inputs.random_bf16(n, k, seed=9)
+    packed, bq, bs = packed_from_oracle(b)
+    m = 8
+    a = torch.zeros((m, k), dtype=torch.bfloat16)
+    picks = [0, 1, 31, 32, 255, 256, 288, 543]
+    for i, p in enumerate(picks):
+        a[i, p] = 1.0
+    got, _ = _run(a, packed, ldc=304)
+    deq_b = oracle.dequant(bq, bs)
+    want = torch.from_numpy(deq_b[:, picks].T.copy()).to(torch.bfloat16).float().numpy()
+    np.testing.assert_array_equal(got, want)
