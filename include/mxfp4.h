@@ -99,8 +99,9 @@ MXFP4_API mxfp4_status mxfp4_prepack_b(const void* b_fp4, const void* b_scale, i
                              size_t b_packed_bytes, void* stream);
 
 /*
- * Workspace bytes mxfp4_gemm needs for this shape (0 for m <= 64, where
- * quantized A never leaves shared memory).
+ * Workspace bytes mxfp4_gemm needs for this shape: 0 for m <= 32, where
+ * quantized A never leaves shared memory; otherwise the size of A's tiled
+ * operand image (the same formula as mxfp4_prepacked_b_bytes(m, k)).
  */
 MXFP4_API size_t mxfp4_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);
 
@@ -113,9 +114,12 @@ MXFP4_API size_t mxfp4_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);
  *   c_bf16   : bf16 [m, n], row stride ldc elements (written, not read)
  *   workspace: device scratch of at least mxfp4_gemm_workspace_bytes(m,n,k)
  *              bytes (may be NULL when that is 0); 16-byte aligned.
- * m <= 64: one launch; A is quantized inside the GEMM kernel.  m > 64: a
+ * m <= 32: one launch; A is quantized inside the GEMM kernel.  m > 32: a
  * quantization launch writes A's operand image into the workspace and the
- * GEMM launch reads it (programmatic dependent launch overlaps the two).
+ * GEMM launch reads it; the GEMM is a programmatic dependent launch that
+ * streams its first weight tiles while the quantization runs.  When K is
+ * split across a thread-block cluster, partial sums are added in a fixed
+ * order, so results are bitwise reproducible.
  * Preconditions: m, n > 0, k > 0, k % 32 == 0, lda >= k, lda % 8 == 0,
  * ldc >= n, ldc % 8 == 0, a_bf16 / b_packed / c_bf16 16-byte aligned.
  */

@@ -5,7 +5,7 @@
 
 #include <cstdint>
 
-#include "../../include/mxfp4.h"
+#include "mxfp4.h"
 #include "mxfp4_device.cuh"
 #include "mxfp4_launch.h"
 

@@ -6,20 +6,29 @@
 //   C[i,j] = bf16( sum_kb 2^(sa[i,kb]-127) 2^(sb[j,kb]-127) sum_t a[i,32kb+t] b[j,32kb+t] )
 //
 // One CTA computes a 128 x BN accumulator tile in tensor memory.  The MMA's
-// 128-row operand ("MMA-A") always comes from a tiled operand image through
-// bulk copies.  Two modes:
-//   swap-AB, fused (m <= 64): MMA-A = the prepacked weight image (n on the
+// 128-row operand ("MMA-A") comes from a tiled operand image through bulk
+// copies.  Three modes:
+//   kFusedSwap (m <= 32): swap-AB.  MMA-A = prepacked weights (n on the
 //     128-row side); MMA-B = the activations, quantized by producer warps
-//     straight from bf16 into shared memory in the MMA layout (quantized A
-//     never reaches HBM); BN = m padded to 16/32/64.
-//   plain (m > 64): MMA-A = the activation image written by
-//     quant_image_kernel into the workspace; MMA-B = BN/128 weight tiles.
-// K may be split across the CTAs of a thread-block cluster; their fp32
-// partial tiles are summed in a fixed order through distributed shared memory.
+//     from bf16 straight into shared memory in the MMA operand and scale
+//     layouts, so quantized A never reaches HBM.  BN = m padded to 16/32.
+//   kImageSwap (32 < m <= 128): swap-AB; MMA-B = the first BN rows of the
+//     activation image that quant_image_kernel wrote into the workspace.
+//   kImagePlain (m > 128): MMA-A = activation image, MMA-B = BN/128 weight
+//     tiles.
+// In the image modes the GEMM is launched as a programmatic dependent of the
+// quantization kernel: it prefetches the weight stages first and waits for
+// the activation image only before loading it.
+//
+// K may be split across the CTAs of a thread-block cluster.  Each CTA pushes
+// the rows of its fp32 partial tile that another rank owns into that rank's
+// shared memory (st.shared::cluster), one cluster barrier follows, and every
+// rank sums its slice in rank order (deterministic) before storing it.
 //
 // Warp roles: warp 0 issues bulk copies; warp 1 owns tensor memory and issues
-// scale-factor copies and MMAs (one thread); warps 2-5 run the epilogue; in
-// the fused mode warps 2-7 also quantize the activations.  Every wait is
+// scale-factor copies and MMAs (one thread); warps 2-5 drain the accumulator;
+// in kFusedSwap warps 2-7 quantize the activations.  All threads stage and
+// store the bf16 output with 16-byte coalesced writes.  Every wait is
 // bounded: a wait that runs out sets a device flag and the CTA winds down.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -32,29 +41,34 @@ namespace mxfp4 {
 
 __device__ int g_timeout_flag = 0;
 
-constexpr uint64_t kWaitLimitNs = 1000000000ull;    // 1 s for a pipeline wait
-constexpr uint64_t kDrainLimitNs = 20000000ull;     // 20 ms when winding down after a timeout
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s for a pipeline wait
+constexpr uint64_t kDrainLimitNs = 20000000ull;   // 20 ms when winding down after a timeout
 constexpr int kStages = 4;
 constexpr int kQuantWarps = 6;
+
+enum GemmMode : int { kFusedSwap = 0, kImageSwap = 1, kImagePlain = 2 };
 
 struct GemmArgs {
   const uint8_t* a_img;  // MMA-A operand image
   int64_t a_rows;        // rows of the matrix in a_img
-  const uint8_t* b_img;  // MMA-B weight image (plain mode)
+  const uint8_t* b_img;  // MMA-B operand image (image modes)
   int64_t b_rows;        // rows of the matrix in b_img
-  const uint16_t* act;   // bf16 activations (fused mode)
+  const uint16_t* act;   // bf16 activations (kFusedSwap)
   int64_t lda;
   int64_t m, n, k;
-  int64_t kt_count;      // K tiles of 256
+  int64_t kt_count;  // K tiles of 256
   __nv_bfloat16* c;
   int64_t ldc;
   int split;
 };
 
-template <int BN, bool kFused>
+template <int BN, int kMode>
 struct Cfg {
+  static constexpr bool kFused = kMode == kFusedSwap;
+  static constexpr bool kSwap = kMode != kImagePlain;
   static constexpr int kThreads = kFused ? 32 * (2 + kQuantWarps) : 32 * 6;
-  static constexpr int kBTiles = kFused ? 1 : BN / 128;           // weight tiles per stage (plain)
+  static constexpr int kBTiles = (BN + 127) / 128;          // image tiles feeding MMA-B per stage
+  static constexpr int kBRowsPerTile = BN < 128 ? BN : 128;  // rows taken from each of them
   static constexpr int kBDataBytes = BN * 128;
   static constexpr int kBSfBytes = kBTiles * kTileSfBytes;
   static constexpr int kOffAData = 0;
@@ -63,19 +77,30 @@ struct Cfg {
   static constexpr int kOffBSf = kOffASf + kStages * kTileSfBytes;
   static constexpr int kOffBars = kOffBSf + kStages * kBSfBytes;
   static constexpr int kOffMisc = kOffBars + (2 * kStages + 1) * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
-  static constexpr int kRedStride = BN + 4;                 // fp32 partial tile row stride
-  static_assert(128 * kRedStride * 4 <= kOffBars, "split-K partial tile must fit in the stage buffers");
+  // Split-K partials land in a region of their own: another rank may push its
+  // rows while this CTA's MMAs still read the stage buffers.  The widest
+  // plain-mode tile has no room for it and never splits K.
+  static constexpr bool kSplitOk = !(kMode == kImagePlain && BN == 256);
+  static constexpr int kRedStride = BN + 4;                                  // fp32 partial-row pitch (floats)
+  static constexpr int kRedBytes = kSplitOk ? 128 * kRedStride * 4 : 0;      // [split][128/split][kRedStride]
+  static constexpr int kOffRed = (kOffMisc + 16 + 15) & ~15;
+  static constexpr int kSmemBytes = kOffRed + kRedBytes + 1024;             // + alignment slack
+  // bf16 output staging reuses the stage buffers once the accumulator is complete
+  static constexpr int kStgPitch = kSwap ? 128 : BN + 8;  // elements
+  static constexpr int kStgBytes = (kSwap ? BN : 128) * kStgPitch * 2;
+  static_assert(kStgBytes <= kOffBars, "output staging must fit in the stage buffers");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   // tensor memory: accumulator columns, then per-stage scale-factor columns
   static constexpr int kAccCols = BN;
-  static constexpr int kSfbColsPerGroup = 4 * ((BN + 127) / 128);
+  static constexpr int kSfbColsPerGroup = 4 * kBTiles;
   static constexpr int kSfColsPerStage = 8 + 2 * kSfbColsPerGroup;
   static constexpr int kTmemNeed = kAccCols + kStages * kSfColsPerStage;
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256 : 512;
   static_assert(kTmemNeed <= 512, "tensor memory");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+  static_assert(!kSwap || BN <= 128, "swap-AB keeps the activations in one image tile");
+  static_assert(!kFused || BN <= 8 * kQuantWarps * 8, "quantizer rows");
 };
 
 __device__ __forceinline__ void raise_timeout(volatile int* abort_flag) {
@@ -106,9 +131,9 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int BN, bool kFused>
-__global__ void __launch_bounds__(Cfg<BN, kFused>::kThreads, 1) gemm_kernel(const GemmArgs args) {
-  using C = Cfg<BN, kFused>;
+template <int BN, int kMode>
+__global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const GemmArgs args) {
+  using C = Cfg<BN, kMode>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
@@ -125,15 +150,68 @@ __global__ void __launch_bounds__(Cfg<BN, kFused>::kThreads, 1) gemm_kernel(cons
   const int64_t KT = args.kt_count;
   const int64_t kt_begin = KT * rank / split;
   const int64_t kt_end = KT * (rank + 1) / split;
+  const int nk = (int)(kt_end - kt_begin);
 
+  // ------------------------------------------------ copy issue (warp 0, lane 0)
+  const uint8_t* a_sf_region = args.a_img + image_sf_region(args.a_rows, args.k);
+  const int64_t b_row_tiles = C::kFused ? 0 : ceil_div(args.b_rows, kTileRows);
+  const uint8_t* b_sf_region = C::kFused ? nullptr : args.b_img + image_sf_region(args.b_rows, args.k);
+  auto stage_bytes = [&]() -> uint32_t {
+    uint32_t bytes = kTileDataBytes + kTileSfBytes;
+    if (!C::kFused)
+      for (int t = 0; t < C::kBTiles; ++t)
+        if (b_tile * C::kBTiles + t < b_row_tiles) bytes += C::kBRowsPerTile * 128 + kTileSfBytes;
+    return bytes;
+  };
+  auto issue_a = [&](int64_t kt, int s, uint64_t policy) {
+    const int64_t at = a_tile * KT + kt;
+    bulk_load_hint(smem + C::kOffAData + s * kTileDataBytes, args.a_img + at * kTileDataBytes, kTileDataBytes,
+                   &full[s], policy);
+    bulk_load_hint(smem + C::kOffASf + s * kTileSfBytes, a_sf_region + at * kTileSfBytes, kTileSfBytes, &full[s],
+                   policy);
+  };
+  auto issue_b = [&](int64_t kt, int s, uint64_t policy) {
+    for (int t = 0; t < C::kBTiles; ++t) {
+      const int64_t brt = b_tile * C::kBTiles + t;
+      if (brt >= b_row_tiles) continue;
+      const int64_t bt = brt * KT + kt;
+      bulk_load_hint(smem + C::kOffBData + s * C::kBDataBytes + t * kTileDataBytes,
+                     args.b_img + bt * kTileDataBytes, C::kBRowsPerTile * 128, &full[s], policy);
+      bulk_load_hint(smem + C::kOffBSf + s * C::kBSfBytes + t * kTileSfBytes, b_sf_region + bt * kTileSfBytes,
+                     kTileSfBytes, &full[s], policy);
+    }
+  };
+  // which operand the preceding quantization kernel produces
+  constexpr bool kADependent = kMode == kImagePlain;
+  constexpr bool kBDependent = kMode == kImageSwap;
+
+  uint64_t pol_weights = 0, pol_act = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1 + (kFused ? kQuantWarps * 32 : 0));
+      mbar_init(&full[s], 1 + (C::kFused ? kQuantWarps * 32 : 0));
       mbar_init(&empty[s], 1);
     }
     mbar_init(accum, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // Start the first stages' copies before anything else: the weight stream
+    // is the long pole.  Operands written by the preceding kernel are
+    // requested only after the programmatic-dependency wait.
+    pol_weights = policy_evict_first();
+    pol_act = policy_evict_last();
+    const int pre = nk < kStages ? nk : kStages;
+    for (int i = 0; i < pre; ++i) {
+      mbar_arrive_expect_tx(&full[i], stage_bytes());
+      if (!kADependent) issue_a(kt_begin + i, i, kMode == kImagePlain ? pol_act : pol_weights);
+      if (!C::kFused && !kBDependent) issue_b(kt_begin + i, i, pol_weights);
+    }
+    if (kADependent || kBDependent) {
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) {
+        if (kADependent) issue_a(kt_begin + i, i, pol_act);
+        if (kBDependent) issue_b(kt_begin + i, i, pol_act);
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -145,57 +223,26 @@ __global__ void __launch_bounds__(Cfg<BN, kFused>::kThreads, 1) gemm_kernel(cons
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------ bulk-copy producer
-    if (lane == 0) {
-      const uint64_t policy_stream = policy_evict_first();
-      const uint8_t* a_sf_region = args.a_img + image_sf_region(args.a_rows, args.k);
-      const int64_t b_row_tiles = kFused ? 0 : ceil_div(args.b_rows, kTileRows);
-      const uint8_t* b_sf_region = kFused ? nullptr : args.b_img + image_sf_region(args.b_rows, args.k);
-      uint32_t issued_parity[kStages];
-      bool used[kStages];
-      for (int s = 0; s < kStages; ++s) used[s] = false;
-      if (!kFused) pdl_wait();  // the activation image comes from the preceding kernel
+    // ------------------------------------------- remaining stages (ring reuse)
+    if (lane == 0 && nk > kStages) {
       int s = 0;
-      uint32_t ph = 0;
-      for (int64_t kt = kt_begin; kt < kt_end; ++kt) {
+      uint32_t ph = 1;  // the prologue filled round 0 of every slot
+      for (int64_t kt = kt_begin + kStages; kt < kt_end; ++kt) {
         if (!wait_bounded(&empty[s], ph ^ 1, abort_flag)) break;
-        uint32_t bytes = kTileDataBytes + kTileSfBytes;
-        if (!kFused) {
-          for (int t = 0; t < C::kBTiles; ++t)
-            if (b_tile * C::kBTiles + t < b_row_tiles) bytes += kTileDataBytes + kTileSfBytes;
-        }
-        mbar_arrive_expect_tx(&full[s], bytes);
-        const int64_t at = a_tile * KT + kt;
-        if (kFused) {
-          bulk_load_hint(smem + C::kOffAData + s * kTileDataBytes, args.a_img + at * kTileDataBytes,
-                         kTileDataBytes, &full[s], policy_stream);
-          bulk_load_hint(smem + C::kOffASf + s * kTileSfBytes, a_sf_region + at * kTileSfBytes, kTileSfBytes,
-                         &full[s], policy_stream);
-        } else {
-          bulk_load(smem + C::kOffAData + s * kTileDataBytes, args.a_img + at * kTileDataBytes, kTileDataBytes,
-                    &full[s]);
-          bulk_load(smem + C::kOffASf + s * kTileSfBytes, a_sf_region + at * kTileSfBytes, kTileSfBytes,
-                    &full[s]);
-          for (int t = 0; t < C::kBTiles; ++t) {
-            const int64_t brt = b_tile * C::kBTiles + t;
-            if (brt >= b_row_tiles) continue;
-            const int64_t bt = brt * KT + kt;
-            bulk_load(smem + C::kOffBData + s * C::kBDataBytes + t * kTileDataBytes,
-                      args.b_img + bt * kTileDataBytes, kTileDataBytes, &full[s]);
-            bulk_load(smem + C::kOffBSf + s * C::kBSfBytes + t * kTileSfBytes, b_sf_region + bt * kTileSfBytes,
-                      kTileSfBytes, &full[s]);
-          }
-        }
-        issued_parity[s] = ph;
-        used[s] = true;
+        mbar_arrive_expect_tx(&full[s], stage_bytes());
+        issue_a(kt, s, kMode == kImagePlain ? pol_act : pol_weights);
+        if (!C::kFused) issue_b(kt, s, kMode == kImageSwap ? pol_act : pol_weights);
         if (++s == kStages) {
           s = 0;
           ph ^= 1;
         }
       }
-      if (*abort_flag) {  // let copies already in flight land before the CTA exits
-        for (int t = 0; t < kStages; ++t)
-          if (used[t]) wait_bounded(&full[t], issued_parity[t], abort_flag, kDrainLimitNs);
+    }
+    if (lane == 0 && *abort_flag) {
+      // let copies already in flight land before the CTA exits
+      for (int t = 0; t < kStages && t < nk; ++t) {
+        const int64_t last_use = (nk - 1 - t) / kStages;  // round of the last copy into slot t
+        wait_bounded(&full[t], (uint32_t)(last_use & 1), abort_flag, kDrainLimitNs);
       }
     }
   } else if (warp == 1) {
@@ -215,7 +262,7 @@ __global__ void __launch_bounds__(Cfg<BN, kFused>::kThreads, 1) gemm_kernel(cons
         for (int g = 0; g < 2; ++g) {
           tmem_copy_32x128b_x4(sfa + g * 4, smem_desc(a_sf_s + g * kAtomBytes, 0, 128, kLayoutNoSwizzle));
 #pragma unroll
-          for (int h = 0; h < C::kSfbColsPerGroup / 4; ++h)
+          for (int h = 0; h < C::kBTiles; ++h)
             tmem_copy_32x128b_x4(sfb + g * C::kSfbColsPerGroup + h * 4,
                                  smem_desc(b_sf_s + h * kTileSfBytes + g * kAtomBytes, 0, 128, kLayoutNoSwizzle));
         }
@@ -242,7 +289,7 @@ __global__ void __launch_bounds__(Cfg<BN, kFused>::kThreads, 1) gemm_kernel(cons
     __syncwarp();
   }
 
-  if constexpr (kFused) {
+  if constexpr (C::kFused) {
     // ---------------------------------------- activation quantizers (warps 2-7)
     if (warp >= 2) {
       constexpr int kRowsPerWarp = (BN + kQuantWarps - 1) / kQuantWarps;
@@ -250,17 +297,17 @@ __global__ void __launch_bounds__(Cfg<BN, kFused>::kThreads, 1) gemm_kernel(cons
       int s = 0;
       uint32_t ph = 0;
       for (int64_t kt = kt_begin; kt < kt_end; ++kt) {
-        if (!wait_bounded(&empty[s], ph ^ 1, abort_flag)) break;
-        uint8_t* bd = smem + C::kOffBData + s * C::kBDataBytes;
-        uint8_t* bsf = smem + C::kOffBSf + s * C::kBSfBytes;
         const int64_t col = kt * kTileK + lane * 8;
         uint4 w[kRowsPerWarp];
 #pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i) {
+        for (int i = 0; i < kRowsPerWarp; ++i) {  // loads first: they do not touch the slot
           const int row = qw + i * kQuantWarps;
           w[i] = (row < args.m && col < args.k) ? ldg_nc_v4(args.act + row * args.lda + col)
                                                 : make_uint4(0, 0, 0, 0);
         }
+        if (!wait_bounded(&empty[s], ph ^ 1, abort_flag)) break;
+        uint8_t* bd = smem + C::kOffBData + s * C::kBDataBytes;
+        uint8_t* bsf = smem + C::kOffBSf + s * C::kBSfBytes;
 #pragma unroll
         for (int i = 0; i < kRowsPerWarp; ++i) {
           const int row = qw + i * kQuantWarps;
@@ -282,106 +329,126 @@ __global__ void __launch_bounds__(Cfg<BN, kFused>::kThreads, 1) gemm_kernel(cons
   }
 
   // ------------------------------------------------------------- epilogue
-  float* red = reinterpret_cast<float*>(smem);  // split-K partial tile (stage buffers are idle now)
+  //   red: [split][128/split][kRedStride] fp32 partial rows owned by this rank
+  //   stg: bf16 output tile, [BN][128] (swap-AB: rows are C rows) or [128][BN+8],
+  //        in the stage buffers, which are idle once the accumulator is complete
+  float* red = reinterpret_cast<float*>(smem + C::kOffRed);
+  __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem);
+  const int rows_per_rank = kTileRows / split;
   if (warp >= 2 && warp < 6) {
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // accumulator row = tensor-memory lane
     const bool ok = wait_bounded(accum, 0, abort_flag);
     tc_fence_after();
     if (ok) {
+      const int owner = row / rows_per_rank;
+      const uint32_t dst_local =
+          smem_addr(red + (size_t)(rank * rows_per_rank + (row - owner * rows_per_rank)) * C::kRedStride);
+      const uint32_t dst = split > 1 ? map_cluster(dst_local, (uint32_t)owner) : 0u;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         uint32_t r[16];
         tmem_load_16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c0, r);
         tmem_load_wait();
-        if (split > 1) {
-          float4* dst = reinterpret_cast<float4*>(red + row * C::kRedStride + c0);
+        if (C::kSplitOk && split > 1) {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-        } else if (kFused) {
-          const int64_t n_idx = a_tile * kTileRows + row;
-          if (n_idx < args.n) {
+            st_cluster_f4(dst + (uint32_t)(c0 + 4 * j) * 4u,
+                          make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                      __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
+        } else if (C::kSwap) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int64_t m_idx = c0 + j;
-              if (m_idx < args.m) args.c[m_idx * args.ldc + n_idx] = __float2bfloat16_rn(__uint_as_float(r[j]));
-            }
-          }
+          for (int j = 0; j < 16; ++j) stg[(c0 + j) * C::kStgPitch + row] = __float2bfloat16_rn(__uint_as_float(r[j]));
         } else {
-          const int64_t m_idx = a_tile * kTileRows + row;
-          const int64_t n0 = b_tile * BN + c0;
-          if (m_idx < args.m) {
-            __nv_bfloat16* dst = args.c + m_idx * args.ldc + n0;
-            if (n0 + 16 <= args.n) {
-              uint4 v0, v1;
-              v0.x = bf16x2_bits(__uint_as_float(r[0]), __uint_as_float(r[1]));
-              v0.y = bf16x2_bits(__uint_as_float(r[2]), __uint_as_float(r[3]));
-              v0.z = bf16x2_bits(__uint_as_float(r[4]), __uint_as_float(r[5]));
-              v0.w = bf16x2_bits(__uint_as_float(r[6]), __uint_as_float(r[7]));
-              v1.x = bf16x2_bits(__uint_as_float(r[8]), __uint_as_float(r[9]));
-              v1.y = bf16x2_bits(__uint_as_float(r[10]), __uint_as_float(r[11]));
-              v1.z = bf16x2_bits(__uint_as_float(r[12]), __uint_as_float(r[13]));
-              v1.w = bf16x2_bits(__uint_as_float(r[14]), __uint_as_float(r[15]));
-              reinterpret_cast<uint4*>(dst)[0] = v0;
-              reinterpret_cast<uint4*>(dst)[1] = v1;
-            } else {
-              for (int j = 0; j < 16 && n0 + j < args.n; ++j) dst[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
-            }
-          }
+          uint4 v0, v1;
+          v0.x = bf16x2_bits(__uint_as_float(r[0]), __uint_as_float(r[1]));
+          v0.y = bf16x2_bits(__uint_as_float(r[2]), __uint_as_float(r[3]));
+          v0.z = bf16x2_bits(__uint_as_float(r[4]), __uint_as_float(r[5]));
+          v0.w = bf16x2_bits(__uint_as_float(r[6]), __uint_as_float(r[7]));
+          v1.x = bf16x2_bits(__uint_as_float(r[8]), __uint_as_float(r[9]));
+          v1.y = bf16x2_bits(__uint_as_float(r[10]), __uint_as_float(r[11]));
+          v1.z = bf16x2_bits(__uint_as_float(r[12]), __uint_as_float(r[13]));
+          v1.w = bf16x2_bits(__uint_as_float(r[14]), __uint_as_float(r[15]));
+          uint4* d = reinterpret_cast<uint4*>(stg + row * C::kStgPitch + c0);
+          d[0] = v0;
+          d[1] = v1;
         }
       }
     }
   }
   tc_fence_before();
   __syncthreads();
+  if (warp == 1) {  // the accumulator has been read out
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
 
-  if (split > 1) {
-    // -------------------------- split-K: fixed-order sum over the cluster's partials
-    cluster_sync();
-    const int rows = kTileRows / split;
-    const int row0 = rank * rows;
+  int row_lo = 0, row_hi = kTileRows;  // accumulator rows this CTA stores
+  if (C::kSplitOk && split > 1) {
+    cluster_sync();  // every rank's partial rows have landed in their owner
+    row_lo = rank * rows_per_rank;
+    row_hi = row_lo + rows_per_rank;
     constexpr int kC4 = BN / 4;
-    const uint32_t red_addr = smem_addr(red);
-    for (int g = threadIdx.x; g < rows * kC4; g += C::kThreads) {
-      const int rr = g % rows, c4 = g / rows;
-      const int row = row0 + rr;
-      const uint32_t off = (uint32_t)((row * C::kRedStride + c4 * 4) * 4);
+    for (int g = threadIdx.x; g < rows_per_rank * kC4; g += C::kThreads) {
+      const int rr = g % rows_per_rank, c4 = g / rows_per_rank;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int q = 0; q < split; ++q) {
-        const float4 v = ld_cluster_f4(map_cluster(red_addr, (uint32_t)q) + off);
+      for (int q = 0; q < split; ++q) {  // fixed rank order: deterministic
+        const float4 v = *reinterpret_cast<const float4*>(red + (size_t)(q * rows_per_rank + rr) * C::kRedStride + c4 * 4);
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
         acc.w += v.w;
       }
-      const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
-      if (kFused) {
-        const int64_t n_idx = a_tile * kTileRows + row;
-        if (n_idx < args.n) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int64_t m_idx = c4 * 4 + e;
-            if (m_idx < args.m) args.c[m_idx * args.ldc + n_idx] = __float2bfloat16_rn(vals[e]);
-          }
-        }
+      const int row = row_lo + rr;
+      if (C::kSwap) {
+        stg[(c4 * 4 + 0) * C::kStgPitch + row] = __float2bfloat16_rn(acc.x);
+        stg[(c4 * 4 + 1) * C::kStgPitch + row] = __float2bfloat16_rn(acc.y);
+        stg[(c4 * 4 + 2) * C::kStgPitch + row] = __float2bfloat16_rn(acc.z);
+        stg[(c4 * 4 + 3) * C::kStgPitch + row] = __float2bfloat16_rn(acc.w);
       } else {
-        const int64_t m_idx = a_tile * kTileRows + row;
-        const int64_t n0 = b_tile * BN + c4 * 4;
-        if (m_idx < args.m) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (n0 + e < args.n) args.c[m_idx * args.ldc + n0 + e] = __float2bfloat16_rn(vals[e]);
-        }
+        uint2 v;
+        v.x = bf16x2_bits(acc.x, acc.y);
+        v.y = bf16x2_bits(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(stg + row * C::kStgPitch + c4 * 4) = v;
       }
     }
-    cluster_sync();  // keep every partial tile alive until all ranks have read it
+    __syncthreads();
   }
 
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+  // ------------------------------------------ coalesced 16-byte stores of C
+  if (C::kSwap) {
+    // stg row j = C row j; stg column r = C column a_tile*128 + r
+    const int64_t n0 = a_tile * kTileRows + row_lo;
+    const int jmax = (int)(args.m < BN ? args.m : BN);
+    const int nch = (row_hi - row_lo) / 8;
+    for (int idx = threadIdx.x; idx < jmax * nch; idx += C::kThreads) {
+      const int j = idx / nch, ch = idx % nch;
+      const int64_t n = n0 + ch * 8;
+      const __nv_bfloat16* src = stg + j * C::kStgPitch + row_lo + ch * 8;
+      __nv_bfloat16* dst = args.c + j * args.ldc + n;
+      if (n + 8 <= args.n) {
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+      } else {
+        for (int e = 0; e < 8 && n + e < args.n; ++e) dst[e] = src[e];
+      }
+    }
+  } else {
+    const int64_t m0 = a_tile * kTileRows;
+    const int64_t n0 = b_tile * BN;
+    constexpr int nch = BN / 8;
+    for (int idx = threadIdx.x; idx < (row_hi - row_lo) * nch; idx += C::kThreads) {
+      const int r = row_lo + idx / nch, ch = idx % nch;
+      const int64_t mi = m0 + r;
+      const int64_t n = n0 + ch * 8;
+      if (mi >= args.m || n >= args.n) continue;
+      const __nv_bfloat16* src = stg + r * C::kStgPitch + ch * 8;
+      __nv_bfloat16* dst = args.c + mi * args.ldc + n;
+      if (n + 8 <= args.n) {
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+      } else {
+        for (int e = 0; e < 8 && n + e < args.n; ++e) dst[e] = src[e];
+      }
+    }
   }
 }
 
@@ -402,17 +469,19 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan) {
   const int sms = num_sms();
   const int64_t KT = ceil_div(k, kTileK);
   GemmPlan p{};
-  if (m <= 64) {
+  if (m <= 128) {
     p.swap_ab = true;
-    p.bn = m <= 16 ? 16 : (m <= 32 ? 32 : 64);
+    p.mode = m <= 32 ? kFusedSwap : kImageSwap;
+    p.bn = m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : 128;
     p.grid_x = ceil_div(n, kTileRows);
     int s = 1;
     while (s < 8 && p.grid_x * s * 2 <= sms && KT / (s * 2) >= 1) s *= 2;
     p.split = s;
     p.grid_y = s;
-    p.workspace = 0;
+    p.workspace = p.mode == kFusedSwap ? 0 : (size_t)image_bytes(m, k);
   } else {
     p.swap_ab = false;
+    p.mode = kImagePlain;
     const int64_t mt = ceil_div(m, kTileRows);
     p.bn = (mt * ceil_div(n, 256) >= sms) ? 256 : 128;
     p.grid_x = mt;
@@ -428,14 +497,15 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan) {
   return 0;
 }
 
-template <int BN, bool kFused>
-static cudaError_t launch_one(const GemmPlan& plan, const GemmArgs& args, cudaStream_t stream, bool pdl) {
-  using C = Cfg<BN, kFused>;
+template <int BN, int kMode>
+static cudaError_t launch_one(const GemmPlan& plan, const GemmArgs& args, cudaStream_t stream) {
+  using C = Cfg<BN, kMode>;
+  if (!C::kSplitOk && plan.split > 1) return cudaErrorInvalidConfiguration;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
@@ -454,14 +524,14 @@ static cudaError_t launch_one(const GemmPlan& plan, const GemmArgs& args, cudaSt
     attrs[na].val.clusterDim.z = 1;
     ++na;
   }
-  if (pdl) {
+  if (kMode != kFusedSwap) {  // dependent of the quantization kernel
     attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attrs[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
   cfg.attrs = attrs;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, kFused>, args);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, kMode>, args);
 }
 
 cudaError_t launch_gemm(const GemmPlan& plan, const void* a_bf16, int64_t m, int64_t k, int64_t lda,
@@ -476,26 +546,36 @@ cudaError_t launch_gemm(const GemmPlan& plan, const void* a_bf16, int64_t m, int
   args.ldc = ldc;
   args.split = plan.split;
   args.lda = lda;
-  if (plan.swap_ab) {
+  if (plan.mode == kFusedSwap) {
     args.a_img = static_cast<const uint8_t*>(b_image);
     args.a_rows = n;
     args.act = static_cast<const uint16_t*>(a_bf16);
     switch (plan.bn) {
-      case 16: return launch_one<16, true>(plan, args, stream, false);
-      case 32: return launch_one<32, true>(plan, args, stream, false);
-      case 64: return launch_one<64, true>(plan, args, stream, false);
+      case 16: return launch_one<16, kFusedSwap>(plan, args, stream);
+      case 32: return launch_one<32, kFusedSwap>(plan, args, stream);
       default: return cudaErrorInvalidValue;
     }
   }
   cudaError_t e = launch_quant_image(a_bf16, m, k, lda, workspace, stream);
   if (e != cudaSuccess) return e;
+  if (plan.mode == kImageSwap) {
+    args.a_img = static_cast<const uint8_t*>(b_image);
+    args.a_rows = n;
+    args.b_img = static_cast<const uint8_t*>(workspace);
+    args.b_rows = m;
+    switch (plan.bn) {
+      case 64: return launch_one<64, kImageSwap>(plan, args, stream);
+      case 128: return launch_one<128, kImageSwap>(plan, args, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   args.a_img = static_cast<const uint8_t*>(workspace);
   args.a_rows = m;
   args.b_img = static_cast<const uint8_t*>(b_image);
   args.b_rows = n;
   switch (plan.bn) {
-    case 128: return launch_one<128, false>(plan, args, stream, true);
-    case 256: return launch_one<256, false>(plan, args, stream, true);
+    case 128: return launch_one<128, kImagePlain>(plan, args, stream);
+    case 256: return launch_one<256, kImagePlain>(plan, args, stream);
     default: return cudaErrorInvalidValue;
   }
 }

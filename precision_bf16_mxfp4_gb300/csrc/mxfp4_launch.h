@@ -24,7 +24,8 @@ cudaError_t launch_prepack(const void* bq, const void* bs, int64_t n, int64_t k,
 
 // GEMM execution plan chosen from (m, n, k) and the device.
 struct GemmPlan {
-  bool swap_ab;        // weights on the MMA's 128-row side, activations quantized in-kernel
+  int mode;            // 0: swap-AB, A quantized in the GEMM; 1: swap-AB on A's image; 2: A image x weights
+  bool swap_ab;        // weights on the MMA's 128-row side
   int bn;              // MMA N: padded m (swap) or the n tile (no swap)
   int split;           // CTAs per cluster splitting K
   int64_t grid_x;      // 128-row tiles of the MMA-A operand

@@ -59,6 +59,9 @@ template <bool kHw>
 __global__ void __launch_bounds__(kQuantThreads)
     quant_image_kernel(const uint16_t* __restrict__ a, int64_t m, int64_t k, int64_t lda,
                        uint8_t* __restrict__ img) {
+  // Let the dependent GEMM launch now: it prefetches weights and waits for
+  // this grid's completion before it reads the image.
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t kt_count = ceil_div(k, kTileK);
   const int64_t total = m * kt_count;
@@ -91,8 +94,6 @@ __global__ void __launch_bounds__(kQuantThreads)
       }
     }
   }
-  // The GEMM that consumes the image may start its prologue now.
-  pdl_launch_dependents();
 }
 
 // Linear MXFP4 B (q [n,k/2], scale [n,k/32]) -> tiled image; one thread per

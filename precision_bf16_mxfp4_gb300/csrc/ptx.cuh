@@ -171,13 +171,10 @@ __device__ __forceinline__ uint32_t map_cluster(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float4 ld_cluster_f4(uint32_t caddr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(caddr)
+__device__ __forceinline__ void st_cluster_f4(uint32_t caddr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(caddr), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
                : "memory");
-  return v;
 }
 
 // ------------------------------------------------ programmatic dependent launch

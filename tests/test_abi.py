@@ -73,12 +73,13 @@ def test_prepacked_size_rejects_bad_shapes():
     assert mx.mxfp4_prepacked_b_bytes(16, -32) == 0
 
 
-@pytest.mark.parametrize("m,n,k", [(4, 2880, 512), (32, 4096, 512), (16, 2112, 7168), (64, 7168, 2048)])
+@pytest.mark.parametrize("m,n,k", [(4, 2880, 512), (32, 4096, 512), (16, 2112, 7168), (1, 1, 32)])
 def test_small_m_needs_no_workspace(m, n, k):
     assert mx.mxfp4_gemm_workspace_bytes(m, n, k) == 0
 
 
-@pytest.mark.parametrize("m,n,k", [(256, 3072, 1536), (4096, 7168, 2048), (65, 8, 32)])
+@pytest.mark.parametrize("m,n,k", [(64, 7168, 2048), (33, 100, 64), (256, 3072, 1536), (4096, 7168, 2048),
+                                   (65, 8, 32)])
 def test_large_m_workspace_is_the_activation_image(m, n, k):
     assert mx.mxfp4_gemm_workspace_bytes(m, n, k) == _image_bytes(m, k)
 
@@ -97,6 +98,7 @@ def test_gemm_rejects_bad_arguments_without_a_gpu():
     assert mx.mxfp4_gemm(None, 4, 64, 64, fake, 16, fake, 16, None, 0, None) == E       # null A
     assert mx.mxfp4_gemm(P(0x10008), 4, 64, 64, fake, 16, fake, 16, None, 0, None) == E  # unaligned A
     assert mx.mxfp4_gemm(fake, 256, 64, 64, fake, 16, fake, 16, None, 0, None) == _lib.MXFP4_ERR_WORKSPACE
+    assert mx.mxfp4_gemm(fake, 33, 64, 64, fake, 16, fake, 16, fake, 100, None) == _lib.MXFP4_ERR_WORKSPACE
 
 
 def test_quant_and_prepack_reject_bad_arguments_without_a_gpu():
