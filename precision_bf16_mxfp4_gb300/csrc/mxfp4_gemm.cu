@@ -41,8 +41,10 @@ namespace mxfp4 {
 
 __device__ int g_timeout_flag = 0;
 
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s for a pipeline wait
-constexpr uint64_t kDrainLimitNs = 20000000ull;   // 20 ms when winding down after a timeout
+// Wait limits in SM clock cycles (read with clock64, which costs a few
+// cycles, unlike the global timer): 2^31 cycles is about 1 s at 2 GHz.
+constexpr long long kWaitLimitCycles = 1ll << 31;
+constexpr long long kDrainLimitCycles = 1ll << 25;  // ~20 ms when winding down after a timeout
 constexpr int kStages = 4;
 constexpr int kQuantWarps = 6;
 
@@ -111,14 +113,14 @@ __device__ __forceinline__ void raise_timeout(volatile int* abort_flag) {
 // Wait for phase `parity` of `bar`; false if the CTA is aborting or the
 // wait ran past its limit (which starts the abort).
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                             uint64_t limit_ns = kWaitLimitNs) {
+                                             long long limit_cycles = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63) == 0) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > limit_ns) {
+      if (clock64() - t0 > limit_cycles) {
         raise_timeout(abort_flag);
         return false;
       }
@@ -242,7 +244,7 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
       // let copies already in flight land before the CTA exits
       for (int t = 0; t < kStages && t < nk; ++t) {
         const int64_t last_use = (nk - 1 - t) / kStages;  // round of the last copy into slot t
-        wait_bounded(&full[t], (uint32_t)(last_use & 1), abort_flag, kDrainLimitNs);
+        wait_bounded(&full[t], (uint32_t)(last_use & 1), abort_flag, kDrainLimitCycles);
       }
     }
   } else if (warp == 1) {
