@@ -127,6 +127,33 @@ MXFP4_API mxfp4_status mxfp4_gemm(const void* a_bf16, int64_t m, int64_t k, int6
                         void* c_bf16, int64_t ldc, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Size of the scratch array built into the library for mxfp4_gemm_noalloc.
+ */
+#define MXFP4_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/*
+ * mxfp4_gemm_noalloc -- the same operation, arguments and results as
+ * mxfp4_gemm, for callers that cannot allocate device memory or pass a
+ * workspace (for example a plugin whose host interface has no scratch
+ * argument, or an engine that has committed all device memory up front).
+ * The pages have no counterpart to this entry point.
+ *   Scratch: a device array of MXFP4_NOALLOC_SCRATCH_BYTES (8 MiB) inside
+ *   the library, held by every device that loads it until process exit.
+ *   The call allocates nothing.  A shape that needs more scratch than that
+ *   (mxfp4_gemm_workspace_bytes(m, n, k) > MXFP4_NOALLOC_SCRATCH_BYTES) is
+ *   rejected with MXFP4_ERR_WORKSPACE before anything is enqueued.
+ *   The first call on a device that needs scratch looks up the array's
+ *   device address with that device current (once per device); make that
+ *   first call before any stream capture.
+ *   All calls on a device share the one array: calls that may overlap on
+ *   the GPU (unordered streams) race; calls ordered in one stream do not.
+ *   Each call rewrites the scratch it uses; nothing needs to start at zero.
+ */
+MXFP4_API mxfp4_status mxfp4_gemm_noalloc(const void* a_bf16, int64_t m, int64_t k, int64_t lda,
+                                          const void* b_packed, int64_t n, void* c_bf16, int64_t ldc,
+                                          void* stream);
+
+/*
  * mxfp4_device_status -- synchronize `stream`, then report and clear the
  * device-side watchdog flag: MXFP4_ERR_TIMEOUT if any kernel of this
  * library on the current device gave up a bounded pipeline wait since the

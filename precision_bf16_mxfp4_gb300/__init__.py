@@ -19,6 +19,7 @@ from ._lib import (  # noqa: F401  (raw C-ABI names)
     Mxfp4Error,
     mxfp4_device_status,
     mxfp4_gemm,
+    mxfp4_gemm_noalloc,
     mxfp4_gemm_workspace_bytes,
     mxfp4_prepack_b,
     mxfp4_prepacked_b_bytes,
@@ -123,6 +124,25 @@ def gemm(a, packed: PackedB, out=None, workspace=None):
                     ctypes_void(c.data_ptr()), c.stride(0), ctypes_void(ws_ptr), ws_bytes,
                     _stream_handle(a.device))
     _check(st, "mxfp4_gemm")
+    return c
+
+
+def gemm_noalloc(a, packed: PackedB, out=None):
+    """Same as :func:`gemm` through mxfp4_gemm_noalloc: for callers that
+    cannot allocate device memory, the scratch comes from an array built into
+    the library (8 MiB per device); larger shapes raise Mxfp4Error."""
+    torch = _torch()
+    _require_cuda(a, "a")
+    if a.dtype != torch.bfloat16 or a.dim() != 2 or a.stride(1) != 1:
+        raise ValueError("a must be a 2-D bf16 tensor with unit column stride")
+    m, k = a.shape
+    if k != packed.k:
+        raise ValueError("a and packed B disagree on k")
+    n = packed.n
+    c = out if out is not None else torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    st = mxfp4_gemm_noalloc(ctypes_void(a.data_ptr()), m, k, a.stride(0), ctypes_void(packed.buf.data_ptr()), n,
+                            ctypes_void(c.data_ptr()), c.stride(0), _stream_handle(a.device))
+    _check(st, "mxfp4_gemm_noalloc")
     return c
 
 

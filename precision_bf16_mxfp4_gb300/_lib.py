@@ -25,8 +25,11 @@ MXFP4_ERR_TIMEOUT = 5
 
 EXPORTED = (
     "mxfp4_status_string", "mxfp4_version", "mxfp4_quant", "mxfp4_prepacked_b_bytes", "mxfp4_prepack_b",
-    "mxfp4_gemm_workspace_bytes", "mxfp4_gemm", "mxfp4_device_status",
+    "mxfp4_gemm_workspace_bytes", "mxfp4_gemm", "mxfp4_gemm_noalloc", "mxfp4_device_status",
 )
+
+# size of the scratch array compiled into the library for mxfp4_gemm_noalloc
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class Mxfp4Error(RuntimeError):
@@ -66,6 +69,8 @@ def load(build_if_missing: bool = True):
         lib.mxfp4_gemm_workspace_bytes.restype = sz
         lib.mxfp4_gemm.argtypes = [p, i64, i64, i64, p, i64, p, i64, p, sz, p]
         lib.mxfp4_gemm.restype = i32
+        lib.mxfp4_gemm_noalloc.argtypes = [p, i64, i64, i64, p, i64, p, i64, p]
+        lib.mxfp4_gemm_noalloc.restype = i32
         lib.mxfp4_device_status.argtypes = [p]
         lib.mxfp4_device_status.restype = i32
         _lib = lib
@@ -102,6 +107,10 @@ def mxfp4_gemm_workspace_bytes(m, n, k) -> int:
 
 def mxfp4_gemm(a_bf16, m, k, lda, b_packed, n, c_bf16, ldc, workspace, workspace_bytes, stream) -> int:
     return int(load().mxfp4_gemm(a_bf16, m, k, lda, b_packed, n, c_bf16, ldc, workspace, workspace_bytes, stream))
+
+
+def mxfp4_gemm_noalloc(a_bf16, m, k, lda, b_packed, n, c_bf16, ldc, stream) -> int:
+    return int(load().mxfp4_gemm_noalloc(a_bf16, m, k, lda, b_packed, n, c_bf16, ldc, stream))
 
 
 def mxfp4_device_status(stream) -> int:
