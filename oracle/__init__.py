@@ -86,7 +86,7 @@ def _bf16_bits(a) -> np.ndarray:
 
 
 def block_exponent(block_bits) -> int:
-    """ub of one block (page 4 "MXFP4 quantization": amax round-up, -2, clamp)."""
+    """ub of one block (submission 694791 "MXFP4 quantization": amax round-up, -2, clamp)."""
     b = _bf16_bits(block_bits)
     return int(_load().oracle_block_exponent(_ptr(b), b.size))
 
@@ -113,7 +113,7 @@ def encode_many(x_bits, ub) -> np.ndarray:
 
 
 def quant(a_bits, m: int | None = None, k: int | None = None):
-    """bf16 [m,k] -> (fp4x2 [m,k/2] u8, e8m0 [m,k/32] u8) (page 4 quantizer, page 1 packing)."""
+    """bf16 [m,k] -> (fp4x2 [m,k/2] u8, e8m0 [m,k/32] u8) (submission 694791 quantizer and packing)."""
     a = _bf16_bits(a_bits)
     if a.ndim != 2:
         raise ValueError("A must be 2-D")
@@ -137,7 +137,7 @@ def dequant(q: np.ndarray, s: np.ndarray) -> np.ndarray:
 
 
 def gemm(aq, a_s, bq, b_s) -> np.ndarray:
-    """C = deq(A) . deq(B)^T in fp64 (page 1 `tl.dot_scaled` semantics)."""
+    """C = deq(A) . deq(B)^T in fp64 (submission 752099 `tl.dot_scaled` semantics)."""
     aq = np.ascontiguousarray(aq, np.uint8)
     a_s = np.ascontiguousarray(a_s, np.uint8)
     bq = np.ascontiguousarray(bq, np.uint8)
@@ -169,7 +169,7 @@ def gemm_via_dequant(aq, a_s, bq, b_s) -> np.ndarray:
     """Same definition as :func:`gemm`, with the fp64 sum taken by numpy's matmul.
 
     The products deq(A)[i,k]*deq(B)[j,k] and their fp64 sum are the definition
-    on page 1 (`tl.dot_scaled`); a library matmul only changes the fp64
+    of submission 752099 (`tl.dot_scaled`); a library matmul only changes the fp64
     summation order.  Used where the plain loop would take minutes.
     """
     return dequant(aq, a_s) @ dequant(bq, b_s).T

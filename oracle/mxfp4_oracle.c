@@ -8,16 +8,16 @@
  * It shares no code, header, table or constant with the CUDA sources.
  *
  * Sources, all on the "kernelbot amd-mxfp4-mm" submission pages:
- *   - block scale rule: page 4 (submission 694791), "MXFP4 quantization:
+ *   - block scale rule: submission 694791, "MXFP4 quantization:
  *     bf16 -> fp4(e2m1) + e8m0 block scales", the amax / round-up / -2 /
- *     clamp / +127 steps; page 1 (submission 752099) `_bf16_to_fp4_hw`,
+ *     clamp / +127 steps; submission 752099 `_bf16_to_fp4_hw`,
  *     which reads the exponent field instead of taking floor(log2);
- *   - element encoding: page 4, same section: scale the element by
+ *   - element encoding: submission 694791, same section: scale the element by
  *     2^(-ub), round to the e2m1 grid with ties to even, saturate at 6.0,
  *     keep the sign as bit 3;
- *   - packing: page 4, same section: two codes per byte, even K index in
+ *   - packing: submission 694791, same section: two codes per byte, even K index in
  *     the low nibble;
- *   - GEMM semantics: page 1 `tl.dot_scaled(a, a_scale, "e2m1", b,
+ *   - GEMM semantics: submission 752099 `tl.dot_scaled(a, a_scale, "e2m1", b,
  *     b_scale, "e2m1", acc)` -- a dequantize-then-multiply product.
  *
  * Arithmetic is fp64 throughout.  Every quantity the quantizer forms is
@@ -41,7 +41,7 @@
 #include <string.h>
 
 /* The eight non-negative e2m1 magnitudes, indexed by the 3-bit code
- * (exponent bits 2..1, mantissa bit 0).  Page 4, "MXFP4 quantization". */
+ * (exponent bits 2..1, mantissa bit 0).  Submission 694791, "MXFP4 quantization". */
 static const double kGrid[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
 
 static double bf16_value(uint16_t h)
@@ -56,8 +56,8 @@ static double bf16_value(uint16_t h)
  * amax is widened to fp32 (exact); its bit pattern gets +0x200000 and is
  * masked with 0xFF800000, which rounds the magnitude up to the next power
  * of two when its fraction is >= 0.75; ub = exponent field - 127 - 2,
- * clamped to [-127, 127].  Page 4 "MXFP4 quantization" (amax, round-up,
- * "-2 accounts for fp4 max 6.0 = 2^2 * 1.5", clamp); page 1
+ * clamped to [-127, 127].  Submission 694791 "MXFP4 quantization" (amax, round-up,
+ * the -2 that puts the block maximum at or below the top of the e2m1 range, clamp); submission 752099
  * `_bf16_to_fp4_hw` for the exponent-field form. */
 int oracle_block_exponent(const uint16_t *x, int64_t count)
 {
@@ -82,7 +82,7 @@ int oracle_block_exponent(const uint16_t *x, int64_t count)
 /* e2m1 magnitude code (0..7) of a non-negative real q.  Values at or above
  * the largest finite e2m1 value saturate to it (code 7, 6.0); below that,
  * the code is the index of the nearest grid value, ties to the even code.
- * Page 4 "MXFP4 quantization" (saturate at >= 6, round to nearest even).
+ * Submission 694791 "MXFP4 quantization" (saturate at >= 6, round to nearest even).
  * For q < 6 every distance below is exact in fp64 whenever it matters: q has
  * at most 8 significant bits, so q - g is exact for q >= 2^-40, and smaller q
  * are unambiguously nearest to 0. */
@@ -117,7 +117,7 @@ int oracle_encode(uint16_t x, int ub)
 /* Quantize A (bf16 [m,k], row stride lda elements) to MXFP4:
  *   q     [m, k/2]  u8, byte j of a row = code(2j) | code(2j+1) << 4
  *   scale [m, k/32] u8, e8m0 = ub + 127
- * k must be a multiple of 32.  Page 4 "MXFP4 quantization" (per-32 block
+ * k must be a multiple of 32.  Submission 694791 "MXFP4 quantization" (per-32 block
  * scale, packing `ev | od << 4`). */
 void oracle_quant(const uint16_t *a, int64_t m, int64_t k, int64_t lda,
                   uint8_t *q, uint8_t *scale)
@@ -173,7 +173,7 @@ static double gemm_entry(const uint8_t *aq, const uint8_t *as,
 }
 
 /* C[m,n] = deq(A) . deq(B)^T in fp64.  A: q [m,k/2] + scale [m,k/32];
- * B: q [n,k/2] + scale [n,k/32].  Page 1 `tl.dot_scaled` semantics. */
+ * B: q [n,k/2] + scale [n,k/32].  Submission 752099 `tl.dot_scaled` semantics. */
 void oracle_gemm(const uint8_t *aq, const uint8_t *as, const uint8_t *bq,
                  const uint8_t *bs, int64_t m, int64_t n, int64_t k,
                  double *c)

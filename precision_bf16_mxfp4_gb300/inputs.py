@@ -6,8 +6,7 @@ path and the CPU oracle can both be fed from it without sharing any of the
 computation they are compared on.
 
 The shapes are the ones the "kernelbot amd-mxfp4-mm" submission pages
-benchmark (page 1, submission 752099, module docstring "The benchmark shapes
-are:" plus the compute-bound large-M case); the value distributions follow
+benchmark (submission 752099, module docstring listing the benchmark shapes, plus the compute-bound large-M case); the value distributions follow
 the workload recipe stated for each shape below.  The leaderboard's own data
 generator is not available, so these seeded draws stand in for it.
 
