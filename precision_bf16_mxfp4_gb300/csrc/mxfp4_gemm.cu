@@ -20,10 +20,12 @@
 // quantization kernel: it prefetches the weight stages first and waits for
 // the activation image only before loading it.
 //
-// K may be split across the CTAs of a thread-block cluster.  Each CTA pushes
-// the rows of its fp32 partial tile that another rank owns into that rank's
-// shared memory (st.shared::cluster), one cluster barrier follows, and every
-// rank sums its slice in rank order (deterministic) before storing it.
+// K may be split across the S CTAs of a thread-block cluster.  Rank r owns
+// accumulator rows [128r/S, 128(r+1)/S): every rank writes those rows of its
+// fp32 partial into slot r of the owner's shared memory (st.shared::cluster;
+// its own rows locally) and the other ranks arrive on the owner's mbarrier
+// with cluster-scope release, one arrival per warp; the owner adds the S
+// slots in rank order (deterministic) and stores its rows.
 //
 // Warp roles: warp 0 issues bulk copies; warp 1 owns tensor memory and issues
 // scale-factor copies and MMAs (one thread); warps 2-5 drain the accumulator;
@@ -32,6 +34,8 @@
 // bounded: a wait that runs out sets a device flag and the CTA winds down.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <cstdlib>
 
 #include "mxfp4_device.cuh"
 #include "mxfp4_launch.h"
@@ -78,15 +82,16 @@ struct Cfg {
   static constexpr int kOffASf = kOffBData + kStages * kBDataBytes;
   static constexpr int kOffBSf = kOffASf + kStages * kTileSfBytes;
   static constexpr int kOffBars = kOffBSf + kStages * kBSfBytes;
-  static constexpr int kOffMisc = kOffBars + (2 * kStages + 1) * 8;
-  // Split-K partials land in a region of their own: another rank may push its
-  // rows while this CTA's MMAs still read the stage buffers.  The widest
-  // plain-mode tile has no room for it and never splits K.
-  static constexpr bool kSplitOk = !(kMode == kImagePlain && BN == 256);
-  static constexpr int kRedStride = BN + 4;                                  // fp32 partial-row pitch (floats)
-  static constexpr int kRedBytes = kSplitOk ? 128 * kRedStride * 4 : 0;      // [split][128/split][kRedStride]
+  static constexpr int kOffMisc = kOffBars + (2 * kStages + 2) * 8;
+  // K split across a cluster: rank r owns accumulator rows [r*128/S, (r+1)*128/S);
+  // every other rank pushes those rows of its fp32 partial into the owner's
+  // shared memory, in a region of its own (a rank may push while the owner's
+  // MMAs still read the stage buffers).
+  static constexpr int kMaxSplit = (kMode == kImagePlain && BN == 256) ? 1 : 8;
+  static constexpr int kRedStride = BN + 4;  // fp32 partial-row pitch (floats)
+  static constexpr int kRedBytes = kMaxSplit > 1 ? 128 * kRedStride * 4 : 0;  // [S][128/S][kRedStride]
   static constexpr int kOffRed = (kOffMisc + 16 + 15) & ~15;
-  static constexpr int kSmemBytes = kOffRed + kRedBytes + 1024;             // + alignment slack
+  static constexpr int kSmemBytes = kOffRed + kRedBytes + 1024;  // + alignment slack
   // bf16 output staging reuses the stage buffers once the accumulator is complete
   static constexpr int kStgPitch = kSwap ? 128 : BN + 8;  // elements
   static constexpr int kStgBytes = (kSwap ? BN : 128) * kStgPitch * 2;
@@ -128,6 +133,22 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
   }
 }
 
+// Same, acquiring at cluster scope (for phases completed by other CTAs' arrivals).
+__device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        raise_timeout(abort_flag);
+        return false;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -141,6 +162,7 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
   uint64_t* empty = full + kStages;
   uint64_t* accum = empty + kStages;
+  uint64_t* red_full = accum + 1;  // rank 0: all other ranks' partial rows have landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -189,16 +211,12 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
 
   uint64_t pol_weights = 0, pol_act = 0;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1 + (C::kFused ? kQuantWarps * 32 : 0));
-      mbar_init(&empty[s], 1);
-    }
-    mbar_init(accum, 1);
-    *abort_flag = 0;
+    // The weight stream is the long pole: initialize only the stage-full
+    // barriers, start the first stages' copies, then set up the rest.
+    // Operands written by the preceding kernel are requested only after the
+    // programmatic-dependency wait.
+    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1 + (C::kFused ? kQuantWarps * 32 : 0));
     fence_mbar_init();
-    // Start the first stages' copies before anything else: the weight stream
-    // is the long pole.  Operands written by the preceding kernel are
-    // requested only after the programmatic-dependency wait.
     pol_weights = policy_evict_first();
     pol_act = policy_evict_last();
     const int pre = nk < kStages ? nk : kStages;
@@ -207,6 +225,12 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
       if (!kADependent) issue_a(kt_begin + i, i, kMode == kImagePlain ? pol_act : pol_weights);
       if (!C::kFused && !kBDependent) issue_b(kt_begin + i, i, pol_weights);
     }
+    for (int s = 0; s < kStages; ++s) mbar_init(&empty[s], 1);
+    mbar_init(accum, 1);
+    // one arrival per (other rank, warp holding some of this rank's rows)
+    mbar_init(red_full, (uint32_t)((split > 1 ? split - 1 : 1) * (split > 4 ? 1 : 4 / split)));
+    *abort_flag = 0;
+    fence_mbar_init();
     if (kADependent || kBDependent) {
       pdl_wait();
       for (int i = 0; i < pre; ++i) {
@@ -223,6 +247,8 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // rank 0's reduction barrier must be initialized before any rank arrives on it
+  if (split > 1) cluster_arrive_relaxed();
 
   if (warp == 0) {
     // ------------------------------------------- remaining stages (ring reuse)
@@ -293,89 +319,121 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
 
   if constexpr (C::kFused) {
     // ---------------------------------------- activation quantizers (warps 2-7)
+    // The bf16 loads for up to kStages K tiles are in flight at once (a
+    // register ring indexed at compile time), so DRAM latency is paid once,
+    // not once per tile.
     if (warp >= 2) {
       constexpr int kRowsPerWarp = (BN + kQuantWarps - 1) / kQuantWarps;
       const int qw = warp - 2;
-      int s = 0;
-      uint32_t ph = 0;
-      for (int64_t kt = kt_begin; kt < kt_end; ++kt) {
+      uint4 w[kStages][kRowsPerWarp];
+      auto load_tile = [&](int64_t kt, uint4 (&dst)[kRowsPerWarp]) {
         const int64_t col = kt * kTileK + lane * 8;
-        uint4 w[kRowsPerWarp];
-#pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i) {  // loads first: they do not touch the slot
-          const int row = qw + i * kQuantWarps;
-          w[i] = (row < args.m && col < args.k) ? ldg_nc_v4(args.act + row * args.lda + col)
-                                                : make_uint4(0, 0, 0, 0);
-        }
-        if (!wait_bounded(&empty[s], ph ^ 1, abort_flag)) break;
-        uint8_t* bd = smem + C::kOffBData + s * C::kBDataBytes;
-        uint8_t* bsf = smem + C::kOffBSf + s * C::kBSfBytes;
 #pragma unroll
         for (int i = 0; i < kRowsPerWarp; ++i) {
           const int row = qw + i * kQuantWarps;
-          if (row < BN) {  // uniform across the warp
-            uint32_t sbyte;
-            const uint32_t packed = quantize_lane<kUseHardwareCvt>(w[i], sbyte);
-            *reinterpret_cast<uint32_t*>(bd + tile_data_offset(row, lane * 4)) = packed;
-            if ((lane & 3) == 0) bsf[tile_sf_offset(row, lane >> 2)] = (uint8_t)sbyte;
+          dst[i] = (kt < kt_end && row < args.m && col < args.k) ? ldg_nc_v4(args.act + row * args.lda + col)
+                                                                 : make_uint4(0, 0, 0, 0);
+        }
+      };
+#pragma unroll
+      for (int u = 0; u < kStages; ++u) load_tile(kt_begin + u, w[u]);
+      uint32_t ph = 0;
+      bool aborted = false;
+      for (int64_t kt0 = kt_begin; kt0 < kt_end && !aborted; kt0 += kStages) {
+#pragma unroll
+        for (int u = 0; u < kStages; ++u) {
+          const int64_t kt = kt0 + u;
+          if (kt >= kt_end || aborted) continue;
+          const bool slot_free = wait_bounded(&empty[u], ph ^ 1, abort_flag);
+          if (!__all_sync(0xFFFFFFFFu, slot_free)) {  // keep the warp's decision uniform
+            aborted = true;
+            continue;
           }
+          uint8_t* bd = smem + C::kOffBData + u * C::kBDataBytes;
+          uint8_t* bsf = smem + C::kOffBSf + u * C::kBSfBytes;
+#pragma unroll
+          for (int i = 0; i < kRowsPerWarp; ++i) {
+            const int row = qw + i * kQuantWarps;
+            if (row < BN) {  // uniform across the warp
+              uint32_t sbyte;
+              const uint32_t packed = quantize_lane<kUseHardwareCvt>(w[u][i], sbyte);
+              *reinterpret_cast<uint32_t*>(bd + tile_data_offset(row, lane * 4)) = packed;
+              if ((lane & 3) == 0) bsf[tile_sf_offset(row, lane >> 2)] = (uint8_t)sbyte;
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&full[u]);
+          load_tile(kt + kStages, w[u]);  // refill this slot of the ring
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&full[s]);
-        if (++s == kStages) {
-          s = 0;
-          ph ^= 1;
-        }
+        ph ^= 1;
       }
     }
   }
 
   // ------------------------------------------------------------- epilogue
-  //   red: [split][128/split][kRedStride] fp32 partial rows owned by this rank
-  //   stg: bf16 output tile, [BN][128] (swap-AB: rows are C rows) or [128][BN+8],
-  //        in the stage buffers, which are idle once the accumulator is complete
+  //   red: [S][128/S][kRedStride] fp32 rows this rank owns, pushed by rank q
+  //        into slot q (a split cluster);
+  //   stg: bf16 output tile, [BN][128] (swap-AB: rows are C rows) or
+  //        [128][BN+8], in the stage buffers, idle once the accumulator is done.
   float* red = reinterpret_cast<float*>(smem + C::kOffRed);
   __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem);
   const int rows_per_rank = kTileRows / split;
+  const int row_lo = rank * rows_per_rank, row_hi = row_lo + rows_per_rank;  // rows this CTA stores
+  __syncwarp();
+  if (split > 1) cluster_wait();  // every rank's barriers are initialized
   if (warp >= 2 && warp < 6) {
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // accumulator row = tensor-memory lane
+    const int owner = row / rows_per_rank;  // a warp's rows span two owners when each owns 16
     const bool ok = wait_bounded(accum, 0, abort_flag);
     tc_fence_after();
-    if (ok) {
-      const int owner = row / rows_per_rank;
-      const uint32_t dst_local =
-          smem_addr(red + (size_t)(rank * rows_per_rank + (row - owner * rows_per_rank)) * C::kRedStride);
-      const uint32_t dst = split > 1 ? map_cluster(dst_local, (uint32_t)owner) : 0u;
+    // split: every row goes to slot `rank` of its owner's partial buffer (the
+    // owner's own rows through the same path, to its own shared memory)
+    const uint32_t dst =
+        split > 1 ? map_cluster(smem_addr(red + (size_t)(rank * rows_per_rank + (row - owner * rows_per_rank)) *
+                                                     C::kRedStride),
+                                (uint32_t)owner)
+                  : 0u;
+    constexpr int kChunk = BN >= 32 ? 32 : 16;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        uint32_t r[16];
+    for (int c0 = 0; c0 < BN; c0 += kChunk) {
+      uint32_t r[kChunk];
+      if constexpr (kChunk == 32) {
+        tmem_load_32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c0, r);
+      } else {
         tmem_load_16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c0, r);
-        tmem_load_wait();
-        if (C::kSplitOk && split > 1) {
+      }
+      tmem_load_wait();
+      if (!ok) continue;
+      if (split > 1) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            st_cluster_f4(dst + (uint32_t)(c0 + 4 * j) * 4u,
-                          make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                      __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
-        } else if (C::kSwap) {
+        for (int j = 0; j < kChunk; j += 4)
+          st_cluster_f4(dst + (uint32_t)(c0 + j) * 4u,
+                        make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                    __uint_as_float(r[j + 3])));
+      } else if (C::kSwap) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) stg[(c0 + j) * C::kStgPitch + row] = __float2bfloat16_rn(__uint_as_float(r[j]));
-        } else {
-          uint4 v0, v1;
-          v0.x = bf16x2_bits(__uint_as_float(r[0]), __uint_as_float(r[1]));
-          v0.y = bf16x2_bits(__uint_as_float(r[2]), __uint_as_float(r[3]));
-          v0.z = bf16x2_bits(__uint_as_float(r[4]), __uint_as_float(r[5]));
-          v0.w = bf16x2_bits(__uint_as_float(r[6]), __uint_as_float(r[7]));
-          v1.x = bf16x2_bits(__uint_as_float(r[8]), __uint_as_float(r[9]));
-          v1.y = bf16x2_bits(__uint_as_float(r[10]), __uint_as_float(r[11]));
-          v1.z = bf16x2_bits(__uint_as_float(r[12]), __uint_as_float(r[13]));
-          v1.w = bf16x2_bits(__uint_as_float(r[14]), __uint_as_float(r[15]));
-          uint4* d = reinterpret_cast<uint4*>(stg + row * C::kStgPitch + c0);
-          d[0] = v0;
-          d[1] = v1;
+        for (int j = 0; j < kChunk; ++j)
+          stg[(c0 + j) * C::kStgPitch + row] = __float2bfloat16_rn(__uint_as_float(r[j]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < kChunk; j += 8) {
+          uint4 u;
+          u.x = bf16x2_bits(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+          u.y = bf16x2_bits(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+          u.z = bf16x2_bits(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
+          u.w = bf16x2_bits(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
+          *reinterpret_cast<uint4*>(stg + row * C::kStgPitch + c0 + j) = u;
         }
       }
+    }
+    if (split > 1) {
+      // The warp's pushes happen before the cluster-scope release of lane 0
+      // (and of lane 16, when the warp's rows span two owners): one arrival
+      // per warp and remote owner.
+      __syncwarp();
+      const bool first_of_owner = lane == 0 || (rows_per_rank < 32 && lane == 16);
+      if (first_of_owner && owner != rank) mbar_arrive_remote(map_cluster(smem_addr(red_full), (uint32_t)owner));
     }
   }
   tc_fence_before();
@@ -385,17 +443,16 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     tmem_dealloc(tmem, C::kTmemCols);
   }
 
-  int row_lo = 0, row_hi = kTileRows;  // accumulator rows this CTA stores
-  if (C::kSplitOk && split > 1) {
-    cluster_sync();  // every rank's partial rows have landed in their owner
-    row_lo = rank * rows_per_rank;
-    row_hi = row_lo + rows_per_rank;
+  if (split > 1) {
+    // ------------------------- sum this rank's rows over the S partials, in rank order
+    wait_bounded_cluster(red_full, 0, abort_flag);  // the other ranks' rows have landed
     constexpr int kC4 = BN / 4;
     for (int g = threadIdx.x; g < rows_per_rank * kC4; g += C::kThreads) {
       const int rr = g % rows_per_rank, c4 = g / rows_per_rank;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int q = 0; q < split; ++q) {  // fixed rank order: deterministic
-        const float4 v = *reinterpret_cast<const float4*>(red + (size_t)(q * rows_per_rank + rr) * C::kRedStride + c4 * 4);
+      for (int q = 0; q < split; ++q) {
+        const float4 v =
+            *reinterpret_cast<const float4*>(red + (size_t)(q * rows_per_rank + rr) * C::kRedStride + c4 * 4);
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
@@ -408,10 +465,10 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
         stg[(c4 * 4 + 2) * C::kStgPitch + row] = __float2bfloat16_rn(acc.z);
         stg[(c4 * 4 + 3) * C::kStgPitch + row] = __float2bfloat16_rn(acc.w);
       } else {
-        uint2 v;
-        v.x = bf16x2_bits(acc.x, acc.y);
-        v.y = bf16x2_bits(acc.z, acc.w);
-        *reinterpret_cast<uint2*>(stg + row * C::kStgPitch + c4 * 4) = v;
+        uint2 u;
+        u.x = bf16x2_bits(acc.x, acc.y);
+        u.y = bf16x2_bits(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(stg + row * C::kStgPitch + c4 * 4) = u;
       }
     }
     __syncthreads();
@@ -422,7 +479,7 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     // stg row j = C row j; stg column r = C column a_tile*128 + r
     const int64_t n0 = a_tile * kTileRows + row_lo;
     const int jmax = (int)(args.m < BN ? args.m : BN);
-    const int nch = (row_hi - row_lo) / 8;
+    const int nch = rows_per_rank / 8;
     for (int idx = threadIdx.x; idx < jmax * nch; idx += C::kThreads) {
       const int j = idx / nch, ch = idx % nch;
       const int64_t n = n0 + ch * 8;
@@ -438,7 +495,7 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     const int64_t m0 = a_tile * kTileRows;
     const int64_t n0 = b_tile * BN;
     constexpr int nch = BN / 8;
-    for (int idx = threadIdx.x; idx < (row_hi - row_lo) * nch; idx += C::kThreads) {
+    for (int idx = threadIdx.x; idx < rows_per_rank * nch; idx += C::kThreads) {
       const int r = row_lo + idx / nch, ch = idx % nch;
       const int64_t mi = m0 + r;
       const int64_t n = n0 + ch * 8;
@@ -467,8 +524,18 @@ int num_sms() {
   return cached[dev];
 }
 
+// MXFP4_SPLIT_K=<1|2|4|8> overrides the K-split factor the planner picks
+// (clamped to what the shape and the kernel allow); for tests and tuning.
+static int split_override() {
+  const char* v = getenv("MXFP4_SPLIT_K");
+  if (!v) return 0;
+  const int s = atoi(v);
+  return (s == 1 || s == 2 || s == 4 || s == 8) ? s : 0;
+}
+
 int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan) {
   const int sms = num_sms();
+  const int forced = split_override();
   const int64_t KT = ceil_div(k, kTileK);
   GemmPlan p{};
   if (m <= 128) {
@@ -476,8 +543,10 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan) {
     p.mode = m <= 32 ? kFusedSwap : kImageSwap;
     p.bn = m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : 128;
     p.grid_x = ceil_div(n, kTileRows);
+    const int s_max = 8;  // the kernels' kMaxSplit
     int s = 1;
-    while (s < 8 && p.grid_x * s * 2 <= sms && KT / (s * 2) >= 1) s *= 2;
+    while (s < s_max && p.grid_x * s * 2 <= sms && KT / (s * 2) >= 1) s *= 2;
+    if (forced) s = forced <= KT ? forced : 1;
     p.split = s;
     p.grid_y = s;
     p.workspace = p.mode == kFusedSwap ? 0 : (size_t)image_bytes(m, k);
@@ -488,8 +557,10 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan) {
     p.bn = (mt * ceil_div(n, 256) >= sms) ? 256 : 128;
     p.grid_x = mt;
     const int64_t nt = ceil_div(n, p.bn);
+    const int s_max = p.bn == 256 ? 1 : 8;  // the kernels' kMaxSplit
     int s = 1;
-    while (s < 8 && mt * nt * s * 2 <= sms && KT / (s * 2) >= 2) s *= 2;
+    while (s < s_max && mt * nt * s * 2 <= sms && KT / (s * 2) >= 2) s *= 2;
+    if (forced) s = (forced <= KT && forced <= s_max) ? forced : 1;
     p.split = s;
     p.grid_y = nt * s;
     p.workspace = (size_t)image_bytes(m, k);
@@ -502,7 +573,7 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan) {
 template <int BN, int kMode>
 static cudaError_t launch_one(const GemmPlan& plan, const GemmArgs& args, cudaStream_t stream) {
   using C = Cfg<BN, kMode>;
-  if (!C::kSplitOk && plan.split > 1) return cudaErrorInvalidConfiguration;
+  if (plan.split > C::kMaxSplit) return cudaErrorInvalidConfiguration;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);

@@ -156,3 +156,25 @@ def test_prepack_roundtrip_through_gemm_columns():
     deq_b = oracle.dequant(bq, bs)
     want = torch.from_numpy(deq_b[:, picks].T.copy()).to(torch.bfloat16).float().numpy()
     np.testing.assert_array_equal(got, want)
+
+
+SPLIT_CASES = [(4, 256, 1024), (16, 300, 2048), (32, 520, 2080), (64, 384, 2048), (200, 256, 2048)]
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("m,n,k", SPLIT_CASES)
+def test_gemm_every_split_factor(m, n, k, split, monkeypatch):
+    """The planner's K split is overridden (MXFP4_SPLIT_K) to run every cluster
+    size through the reduce-scatter epilogue, including 16-row owners."""
+    monkeypatch.setenv("MXFP4_SPLIT_K", str(split))
+    a = inputs.random_bf16(m, k, seed=m + split)
+    b = inputs.random_bf16(n, k, seed=n + split, std=0.3)
+    packed, bq, bs = packed_from_oracle(b)
+    ldc = n + (8 - n % 8) % 8
+    got, c_full = _run(a, packed, ldc=ldc)
+    assert_close_to_ref(got, _oracle_full(a, bq, bs), what=f"split {split}")
+    a_dev = a.cuda()
+    c1 = mx.gemm(a_dev, packed, out=torch.empty((m, ldc), dtype=torch.bfloat16, device="cuda")[:, :n])
+    c2 = mx.gemm(a_dev, packed, out=torch.empty((m, ldc), dtype=torch.bfloat16, device="cuda")[:, :n])
+    torch.cuda.synchronize()
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
