@@ -16,28 +16,33 @@
 namespace mxfp4 {
 
 // ------------------------------------------------------------ image layout
-// An MXFP4 matrix X[R, K] is stored for the MMA as tiles of 128 rows x 256 K
-// elements.  Data region: tile (rt, kt) at (rt * KT + kt) * 16384 bytes,
-// holding 128 rows of 128 bytes in the 128-byte-swizzled K-major order the
-// MMA descriptor expects (16-byte chunk c of row r sits at chunk c ^ (r & 7)).
-// Scale region (after all data): tile (rt, kt) at (rt * KT + kt) * 1024,
-// two 512-byte atoms (K blocks 0-3, 4-7); inside an atom, row r and block b
-// sit at (r % 32) * 16 + (r / 32) * 4 + b, the 32-lane x 16-byte shape that
-// tcgen05.cp copies into tensor memory.  Rows beyond R and K beyond the
-// matrix are zero in the weight image.
+// An MXFP4 matrix X[R, K] is stored for the MMA as blocks of 128 rows x 256 K
+// elements.  Block (rt, kt) sits at (rt * KT + kt) * 17408 bytes, so the K
+// blocks of one row tile are contiguous and a single bulk copy can move
+// several of them.  Each block holds
+//   bytes [0, 16384): 128 rows of 128 bytes in the 128-byte-swizzled K-major
+//     order the MMA descriptor expects (16-byte chunk c of row r sits at
+//     chunk c ^ (r & 7));
+//   bytes [16384, 17408): the e8m0 scales as two 512-byte atoms (K blocks
+//     0-3, 4-7); inside an atom, row r and block b sit at
+//     (r % 32) * 16 + (r / 32) * 4 + b, the 32-lane x 16-byte shape that
+//     tcgen05.cp copies into tensor memory.
+// Rows beyond R and K beyond the matrix are zero in the weight image.
 constexpr int kTileRows = 128;
 constexpr int kTileK = 256;
 constexpr int kTileDataBytes = 16384;
 constexpr int kTileSfBytes = 1024;
+constexpr int kTileBytes = kTileDataBytes + kTileSfBytes;  // 17 x 1024: blocks stay 1024-byte aligned
 constexpr int kAtomBytes = 512;
 
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 __host__ __device__ inline int64_t image_bytes(int64_t rows, int64_t k) {
-  return ceil_div(rows, kTileRows) * ceil_div(k, kTileK) * (kTileDataBytes + kTileSfBytes);
+  return ceil_div(rows, kTileRows) * ceil_div(k, kTileK) * kTileBytes;
 }
-__host__ __device__ inline int64_t image_sf_region(int64_t rows, int64_t k) {
-  return ceil_div(rows, kTileRows) * ceil_div(k, kTileK) * kTileDataBytes;
+// offset of block (rt, kt) in an image with kt_count K blocks per row tile
+__host__ __device__ inline int64_t image_block(int64_t rt, int64_t kt, int64_t kt_count) {
+  return (rt * kt_count + kt) * kTileBytes;
 }
 // byte of row r (0..127), packed-K byte kb (0..127) inside a data tile
 __host__ __device__ inline int tile_data_offset(int r, int kbyte) {

@@ -6,19 +6,26 @@
 //   C[i,j] = bf16( sum_kb 2^(sa[i,kb]-127) 2^(sb[j,kb]-127) sum_t a[i,32kb+t] b[j,32kb+t] )
 //
 // One CTA computes a 128 x BN accumulator tile in tensor memory.  The MMA's
-// 128-row operand ("MMA-A") comes from a tiled operand image through bulk
-// copies.  Three modes:
+// 128-row operand ("MMA-A") comes from a tiled operand image (see
+// mxfp4_device.cuh) through bulk copies.  Modes:
 //   kFusedSwap (m <= 32): swap-AB.  MMA-A = prepacked weights (n on the
 //     128-row side); MMA-B = the activations, quantized by producer warps
 //     from bf16 straight into shared memory in the MMA operand and scale
 //     layouts, so quantized A never reaches HBM.  BN = m padded to 16/32.
 //   kImageSwap (32 < m <= 128): swap-AB; MMA-B = the first BN rows of the
 //     activation image that quant_image_kernel wrote into the workspace.
-//   kImagePlain (m > 128): MMA-A = activation image, MMA-B = BN/128 weight
-//     tiles.
+//   kImagePlain (m > 128, few tiles): MMA-A = activation image, MMA-B = 128
+//     weight rows.  With at least one 128 x 256 tile per SM the persistent
+//     kernel below takes over.
 // In the image modes the GEMM is launched as a programmatic dependent of the
-// quantization kernel: it prefetches the weight stages first and waits for
+// quantization kernel: it streams its first weight stages first and waits for
 // the activation image only before loading it.
+//
+// Pipeline stages hold kSuperK consecutive K blocks (256 K each) of every
+// operand row tile, so each stage is one bulk copy per row tile: the TMA
+// engine's throughput per SM grows with the size of each copy (about
+// 40 GB/s for 16 KiB copies, 120-160 GB/s for 48-64 KiB ones, measured on
+// GB300), not with the number of copies in flight.
 //
 // K may be split across the S CTAs of a thread-block cluster.  Rank r owns
 // accumulator rows [128r/S, 128(r+1)/S): every rank writes those rows of its
@@ -29,9 +36,8 @@
 //
 // Warp roles: warp 0 issues bulk copies; warp 1 owns tensor memory and issues
 // scale-factor copies and MMAs (one thread); warps 2-5 drain the accumulator;
-// in kFusedSwap warps 2-7 quantize the activations.  All threads stage and
-// store the bf16 output with 16-byte coalesced writes.  Every wait is
-// bounded: a wait that runs out sets a device flag and the CTA winds down.
+// in kFusedSwap warps 2-7 quantize the activations.  Every wait is bounded: a
+// wait that runs out sets a device flag and the CTA winds down.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -49,20 +55,21 @@ __device__ int g_timeout_flag = 0;
 // cycles, unlike the global timer): 2^31 cycles is about 1 s at 2 GHz.
 constexpr long long kWaitLimitCycles = 1ll << 31;
 constexpr long long kDrainLimitCycles = 1ll << 25;  // ~20 ms when winding down after a timeout
-constexpr int kStages = 4;
+constexpr int kSuperK = 2;                          // K blocks per pipeline stage
+constexpr int kStages = 2;                          // stages in the ring
 constexpr int kQuantWarps = 6;
+constexpr int kRing = kSuperK * kStages;            // K blocks in flight
 
 enum GemmMode : int { kFusedSwap = 0, kImageSwap = 1, kImagePlain = 2 };
 
 struct GemmArgs {
   const uint8_t* a_img;  // MMA-A operand image
-  int64_t a_rows;        // rows of the matrix in a_img
   const uint8_t* b_img;  // MMA-B operand image (image modes)
   int64_t b_rows;        // rows of the matrix in b_img
   const uint16_t* act;   // bf16 activations (kFusedSwap)
   int64_t lda;
   int64_t m, n, k;
-  int64_t kt_count;  // K tiles of 256
+  int64_t kt_count;  // K blocks of 256
   __nv_bfloat16* c;
   int64_t ldc;
   int split;
@@ -72,24 +79,24 @@ template <int BN, int kMode>
 struct Cfg {
   static constexpr bool kFused = kMode == kFusedSwap;
   static constexpr bool kSwap = kMode != kImagePlain;
-  static constexpr int kThreads = kFused ? 32 * (2 + kQuantWarps) : 32 * 6;
-  static constexpr int kBTiles = (BN + 127) / 128;          // image tiles feeding MMA-B per stage
-  static constexpr int kBRowsPerTile = BN < 128 ? BN : 128;  // rows taken from each of them
-  static constexpr int kBDataBytes = BN * 128;
-  static constexpr int kBSfBytes = kBTiles * kTileSfBytes;
-  static constexpr int kOffAData = 0;
-  static constexpr int kOffBData = kOffAData + kStages * kTileDataBytes;
-  static constexpr int kOffASf = kOffBData + kStages * kBDataBytes;
-  static constexpr int kOffBSf = kOffASf + kStages * kTileSfBytes;
-  static constexpr int kOffBars = kOffBSf + kStages * kBSfBytes;
+  // warps: 0 and the last one issue bulk copies (even / odd stages), 1 issues
+  // MMAs, 2-5 drain the accumulator, 2-7 quantize A in kFusedSwap
+  static constexpr int kThreads = kFused ? 32 * (3 + kQuantWarps) : 32 * 7;
+  static constexpr int kOddProducerWarp = kThreads / 32 - 1;
+  static constexpr int kBRows = BN;                                    // MMA N (<= 128 here)
+  static constexpr int kABytes = kSuperK * kTileBytes;                 // MMA-A bytes per stage
+  static constexpr int kBBlock = kFused ? BN * 128 + kTileSfBytes : kTileBytes;  // per K block
+  static constexpr int kBSfOffset = kFused ? BN * 128 : kTileDataBytes;          // scales inside a B block
+  static constexpr int kBBytes = kSuperK * kBBlock;                    // MMA-B bytes per stage
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffBars = kOffB + kStages * kBBytes;
   static constexpr int kOffMisc = kOffBars + (2 * kStages + 2) * 8;
-  // K split across a cluster: rank r owns accumulator rows [r*128/S, (r+1)*128/S);
-  // every other rank pushes those rows of its fp32 partial into the owner's
-  // shared memory, in a region of its own (a rank may push while the owner's
-  // MMAs still read the stage buffers).
-  static constexpr int kMaxSplit = (kMode == kImagePlain && BN == 256) ? 1 : 8;
-  static constexpr int kRedStride = BN + 4;  // fp32 partial-row pitch (floats)
-  static constexpr int kRedBytes = kMaxSplit > 1 ? 128 * kRedStride * 4 : 0;  // [S][128/S][kRedStride]
+  // split-K partials of the rows this rank owns land in a region of their own:
+  // another rank may push while this CTA's MMAs still read the stage buffers
+  static constexpr int kMaxSplit = 8;
+  static constexpr int kRedStride = BN + 4;                   // fp32 partial-row pitch (floats)
+  static constexpr int kRedBytes = 128 * kRedStride * 4;      // [S][128/S][kRedStride]
   static constexpr int kOffRed = (kOffMisc + 16 + 15) & ~15;
   static constexpr int kSmemBytes = kOffRed + kRedBytes + 1024;  // + alignment slack
   // bf16 output staging reuses the stage buffers once the accumulator is complete
@@ -97,17 +104,16 @@ struct Cfg {
   static constexpr int kStgBytes = (kSwap ? BN : 128) * kStgPitch * 2;
   static_assert(kStgBytes <= kOffBars, "output staging must fit in the stage buffers");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kBBlock % 1024 == 0, "swizzled operand blocks must stay 1024-byte aligned");
   // tensor memory: accumulator columns, then per-stage scale-factor columns
+  // (8 per K block for A, 8 per K block for B)
   static constexpr int kAccCols = BN;
-  static constexpr int kSfbColsPerGroup = 4 * kBTiles;
-  static constexpr int kSfColsPerStage = 8 + 2 * kSfbColsPerGroup;
+  static constexpr int kSfColsPerStage = kSuperK * 16;
   static constexpr int kTmemNeed = kAccCols + kStages * kSfColsPerStage;
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256 : 512;
   static_assert(kTmemNeed <= 512, "tensor memory");
-  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
-  static_assert(!kSwap || BN <= 128, "swap-AB keeps the activations in one image tile");
-  static_assert(!kFused || BN <= 8 * kQuantWarps * 8, "quantizer rows");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "MMA N");
 };
 
 __device__ __forceinline__ void raise_timeout(volatile int* abort_flag) {
@@ -154,6 +160,18 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Scale factors of one K block (two 512-byte atoms) into 8 tensor-memory columns.
+__device__ __forceinline__ void copy_block_scales(uint32_t tmem_col, uint32_t sf_smem) {
+  tmem_copy_32x128b_x4(tmem_col, smem_desc(sf_smem, 0, 128, kLayoutNoSwizzle));
+  tmem_copy_32x128b_x4(tmem_col + 4, smem_desc(sf_smem + kAtomBytes, 0, 128, kLayoutNoSwizzle));
+}
+
+// K steps of 64 in the K block starting at element kt * 256
+__device__ __forceinline__ int k_steps(int64_t k, int64_t kt) {
+  const int64_t rem = k - kt * kTileK;
+  return rem >= kTileK ? 4 : (int)ceil_div(rem, 64);
+}
+
 template <int BN, int kMode>
 __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const GemmArgs args) {
   using C = Cfg<BN, kMode>;
@@ -162,7 +180,7 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
   uint64_t* empty = full + kStages;
   uint64_t* accum = empty + kStages;
-  uint64_t* red_full = accum + 1;  // rank 0: all other ranks' partial rows have landed
+  uint64_t* red_full = accum + 1;  // the other ranks' partial rows owned by this rank have landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -170,72 +188,59 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   const int split = args.split;
   const int rank = split > 1 ? (int)(blockIdx.y % split) : 0;
   const int64_t a_tile = blockIdx.x;
-  const int64_t b_tile = blockIdx.y / split;
+  const int64_t b_tile = blockIdx.y / split;  // row tile of the MMA-B image (plain mode)
   const int64_t KT = args.kt_count;
   const int64_t kt_begin = KT * rank / split;
   const int64_t kt_end = KT * (rank + 1) / split;
-  const int nk = (int)(kt_end - kt_begin);
+  const int nss = (int)ceil_div(kt_end - kt_begin, kSuperK);  // pipeline stages this CTA runs
 
-  // ------------------------------------------------ copy issue (warp 0, lane 0)
-  const uint8_t* a_sf_region = args.a_img + image_sf_region(args.a_rows, args.k);
-  const int64_t b_row_tiles = C::kFused ? 0 : ceil_div(args.b_rows, kTileRows);
-  const uint8_t* b_sf_region = C::kFused ? nullptr : args.b_img + image_sf_region(args.b_rows, args.k);
-  auto stage_bytes = [&]() -> uint32_t {
-    uint32_t bytes = kTileDataBytes + kTileSfBytes;
-    if (!C::kFused)
-      for (int t = 0; t < C::kBTiles; ++t)
-        if (b_tile * C::kBTiles + t < b_row_tiles) bytes += C::kBRowsPerTile * 128 + kTileSfBytes;
-    return bytes;
-  };
-  auto issue_a = [&](int64_t kt, int s, uint64_t policy) {
-    const int64_t at = a_tile * KT + kt;
-    bulk_load_hint(smem + C::kOffAData + s * kTileDataBytes, args.a_img + at * kTileDataBytes, kTileDataBytes,
-                   &full[s], policy);
-    bulk_load_hint(smem + C::kOffASf + s * kTileSfBytes, a_sf_region + at * kTileSfBytes, kTileSfBytes, &full[s],
-                   policy);
-  };
-  auto issue_b = [&](int64_t kt, int s, uint64_t policy) {
-    for (int t = 0; t < C::kBTiles; ++t) {
-      const int64_t brt = b_tile * C::kBTiles + t;
-      if (brt >= b_row_tiles) continue;
-      const int64_t bt = brt * KT + kt;
-      bulk_load_hint(smem + C::kOffBData + s * C::kBDataBytes + t * kTileDataBytes,
-                     args.b_img + bt * kTileDataBytes, C::kBRowsPerTile * 128, &full[s], policy);
-      bulk_load_hint(smem + C::kOffBSf + s * C::kBSfBytes + t * kTileSfBytes, b_sf_region + bt * kTileSfBytes,
-                     kTileSfBytes, &full[s], policy);
-    }
-  };
-  // which operand the preceding quantization kernel produces
+  // operand written by the preceding quantization kernel
   constexpr bool kADependent = kMode == kImagePlain;
   constexpr bool kBDependent = kMode == kImageSwap;
+  const bool b_valid = !C::kFused && b_tile < ceil_div(args.b_rows, kTileRows);
+  auto stage_kblocks = [&](int ss) -> int {
+    const int64_t left = kt_end - (kt_begin + (int64_t)ss * kSuperK);
+    return left < kSuperK ? (int)left : kSuperK;
+  };
+  auto stage_bytes = [&](int ss) -> uint32_t {
+    const uint32_t cnt = (uint32_t)stage_kblocks(ss);
+    return cnt * kTileBytes + (b_valid ? cnt * kTileBytes : 0u);
+  };
+  auto issue_a = [&](int ss, int s, uint64_t policy) {
+    const int64_t kt0 = kt_begin + (int64_t)ss * kSuperK;
+    bulk_load_hint(smem + C::kOffA + s * C::kABytes, args.a_img + image_block(a_tile, kt0, KT),
+                   (uint32_t)stage_kblocks(ss) * kTileBytes, &full[s], policy);
+  };
+  auto issue_b = [&](int ss, int s, uint64_t policy) {
+    if (!b_valid) return;
+    const int64_t kt0 = kt_begin + (int64_t)ss * kSuperK;
+    bulk_load_hint(smem + C::kOffB + s * C::kBBytes, args.b_img + image_block(b_tile, kt0, KT),
+                   (uint32_t)stage_kblocks(ss) * kTileBytes, &full[s], policy);
+  };
 
-  uint64_t pol_weights = 0, pol_act = 0;
   if (threadIdx.x == 0) {
-    // The weight stream is the long pole: initialize only the stage-full
-    // barriers, start the first stages' copies, then set up the rest.
-    // Operands written by the preceding kernel are requested only after the
-    // programmatic-dependency wait.
-    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1 + (C::kFused ? kQuantWarps * 32 : 0));
-    fence_mbar_init();
-    pol_weights = policy_evict_first();
-    pol_act = policy_evict_last();
-    const int pre = nk < kStages ? nk : kStages;
-    for (int i = 0; i < pre; ++i) {
-      mbar_arrive_expect_tx(&full[i], stage_bytes());
-      if (!kADependent) issue_a(kt_begin + i, i, kMode == kImagePlain ? pol_act : pol_weights);
-      if (!C::kFused && !kBDependent) issue_b(kt_begin + i, i, pol_weights);
+    // The weight stream is the long pole: initialize the barriers and start
+    // stage 0 at once; the odd-stage producer starts stage 1 after the
+    // prologue barrier.  The operand the preceding kernel writes is requested
+    // only after the dependency wait.
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1 + (C::kFused ? kQuantWarps * 32 : 0));
+      mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < kStages; ++s) mbar_init(&empty[s], 1);
     mbar_init(accum, 1);
     // one arrival per (other rank, warp holding some of this rank's rows)
     mbar_init(red_full, (uint32_t)((split > 1 ? split - 1 : 1) * (split > 4 ? 1 : 4 / split)));
     *abort_flag = 0;
     fence_mbar_init();
-    if (kADependent || kBDependent) {
-      pdl_wait();
-      for (int i = 0; i < pre; ++i) {
-        if (kADependent) issue_a(kt_begin + i, i, pol_act);
-        if (kBDependent) issue_b(kt_begin + i, i, pol_act);
+    if (nss > 0) {
+      const uint64_t pol_weights = policy_evict_first(), pol_act = policy_evict_last();
+      mbar_arrive_expect_tx(&full[0], stage_bytes(0));
+      if (!kADependent) issue_a(0, 0, kMode == kImagePlain ? pol_act : pol_weights);
+      if (!C::kFused && !kBDependent) issue_b(0, 0, pol_weights);
+      if (kADependent || kBDependent) {
+        pdl_wait();
+        if (kADependent) issue_a(0, 0, pol_act);
+        if (kBDependent) issue_b(0, 0, pol_act);
       }
     }
   }
@@ -247,70 +252,66 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // rank 0's reduction barrier must be initialized before any rank arrives on it
+  // the owners' reduction barriers must be initialized before any rank arrives on them
   if (split > 1) cluster_arrive_relaxed();
 
-  if (warp == 0) {
-    // ------------------------------------------- remaining stages (ring reuse)
-    if (lane == 0 && nk > kStages) {
-      int s = 0;
-      uint32_t ph = 1;  // the prologue filled round 0 of every slot
-      for (int64_t kt = kt_begin + kStages; kt < kt_end; ++kt) {
-        if (!wait_bounded(&empty[s], ph ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&full[s], stage_bytes());
-        issue_a(kt, s, kMode == kImagePlain ? pol_act : pol_weights);
-        if (!C::kFused) issue_b(kt, s, kMode == kImageSwap ? pol_act : pol_weights);
-        if (++s == kStages) {
-          s = 0;
-          ph ^= 1;
+  if (warp == 0 || warp == C::kOddProducerWarp) {
+    // --------------------------------- bulk-copy producers: one per stage slot
+    // The TMA engine serializes the bulk copies issued by one thread, so the
+    // two slots' copies are issued by two warps and move concurrently.
+    if (lane == 0) {
+      const int slot = warp == 0 ? 0 : 1;
+      const uint64_t pol_weights = policy_evict_first(), pol_act = policy_evict_last();
+      const uint64_t pol_a = kMode == kImagePlain ? pol_act : pol_weights;
+      const uint64_t pol_b = kMode == kImageSwap ? pol_act : pol_weights;
+      bool waited_dependency = slot == 0;  // thread 0 already waited in the prologue
+      for (int ss = slot; ss < nss; ss += kStages) {
+        if (ss == 0) continue;  // issued in the prologue
+        const int s = ss % kStages;
+        if (!wait_bounded(&empty[s], (uint32_t)(((ss / kStages) & 1) ^ 1), abort_flag)) break;
+        mbar_arrive_expect_tx(&full[s], stage_bytes(ss));
+        if (!kADependent) issue_a(ss, s, pol_a);
+        if (!C::kFused && !kBDependent) issue_b(ss, s, pol_b);
+        if (kADependent || kBDependent) {
+          if (!waited_dependency) {
+            pdl_wait();
+            waited_dependency = true;
+          }
+          if (kADependent) issue_a(ss, s, pol_a);
+          if (kBDependent) issue_b(ss, s, pol_b);
         }
       }
-    }
-    if (lane == 0 && *abort_flag) {
-      // let copies already in flight land before the CTA exits
-      for (int t = 0; t < kStages && t < nk; ++t) {
-        const int64_t last_use = (nk - 1 - t) / kStages;  // round of the last copy into slot t
-        wait_bounded(&full[t], (uint32_t)(last_use & 1), abort_flag, kDrainLimitCycles);
+      if (*abort_flag && slot < nss) {  // let this slot's copies in flight land before the CTA exits
+        const int last = slot + ((nss - 1 - slot) / kStages) * kStages;
+        wait_bounded(&full[slot], (uint32_t)((last / kStages) & 1), abort_flag, kDrainLimitCycles);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int s = 0;
-      uint32_t ph = 0;
       bool accumulate = false;
-      for (int64_t kt = kt_begin; kt < kt_end; ++kt) {
-        if (!wait_bounded(&full[s], ph, abort_flag)) break;
+      for (int ss = 0; ss < nss; ++ss) {
+        const int s = ss % kStages;
+        if (!wait_bounded(&full[s], (uint32_t)((ss / kStages) & 1), abort_flag)) break;
         tc_fence_after();
         const uint32_t sfa = tmem + C::kAccCols + s * C::kSfColsPerStage;
-        const uint32_t sfb = sfa + 8;
-        const uint32_t a_sf_s = smem_addr(smem + C::kOffASf + s * kTileSfBytes);
-        const uint32_t b_sf_s = smem_addr(smem + C::kOffBSf + s * C::kBSfBytes);
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          tmem_copy_32x128b_x4(sfa + g * 4, smem_desc(a_sf_s + g * kAtomBytes, 0, 128, kLayoutNoSwizzle));
-#pragma unroll
-          for (int h = 0; h < C::kBTiles; ++h)
-            tmem_copy_32x128b_x4(sfb + g * C::kSfbColsPerGroup + h * 4,
-                                 smem_desc(b_sf_s + h * kTileSfBytes + g * kAtomBytes, 0, 128, kLayoutNoSwizzle));
-        }
-        const uint32_t a_s = smem_addr(smem + C::kOffAData + s * kTileDataBytes);
-        const uint32_t b_s = smem_addr(smem + C::kOffBData + s * C::kBDataBytes);
-        const int64_t rem = args.k - kt * kTileK;
-        const int kk_count = rem >= kTileK ? 4 : (int)ceil_div(rem, 64);
-        for (int kk = 0; kk < kk_count; ++kk) {
-          const int g = kk >> 1;
-          const uint32_t id = (uint32_t)(kk & 1) * 2;
-          mma_mxf4(tmem, smem_desc(a_s + kk * 32, 0, 1024, kLayoutSwizzle128),
-                   smem_desc(b_s + kk * 32, 0, 1024, kLayoutSwizzle128), idesc_mxf4(128, BN, id, id),
-                   sfa + g * 4, sfb + g * C::kSfbColsPerGroup, accumulate ? 1u : 0u);
-          accumulate = true;
+        const uint32_t sfb = sfa + kSuperK * 8;
+        const int cnt = stage_kblocks(ss);
+        for (int j = 0; j < cnt; ++j) {
+          const uint32_t a_blk = smem_addr(smem + C::kOffA + s * C::kABytes + j * kTileBytes);
+          const uint32_t b_blk = smem_addr(smem + C::kOffB + s * C::kBBytes + j * C::kBBlock);
+          copy_block_scales(sfa + j * 8, a_blk + kTileDataBytes);
+          copy_block_scales(sfb + j * 8, b_blk + C::kBSfOffset);
+          const int steps = k_steps(args.k, kt_begin + (int64_t)ss * kSuperK + j);
+          for (int kk = 0; kk < steps; ++kk) {
+            const uint32_t id = (uint32_t)(kk & 1) * 2;
+            mma_mxf4(tmem, smem_desc(a_blk + kk * 32, 0, 1024, kLayoutSwizzle128),
+                     smem_desc(b_blk + kk * 32, 0, 1024, kLayoutSwizzle128), idesc_mxf4(128, C::kBRows, id, id),
+                     sfa + j * 8 + (kk >> 1) * 4, sfb + j * 8 + (kk >> 1) * 4, accumulate ? 1u : 0u);
+            accumulate = true;
+          }
         }
         mma_commit(&empty[s]);
-        if (++s == kStages) {
-          s = 0;
-          ph ^= 1;
-        }
       }
       mma_commit(accum);  // fires once every MMA above has completed
     }
@@ -319,14 +320,15 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
 
   if constexpr (C::kFused) {
     // ---------------------------------------- activation quantizers (warps 2-7)
-    // The bf16 loads for up to kStages K tiles are in flight at once (a
-    // register ring indexed at compile time), so DRAM latency is paid once,
-    // not once per tile.
-    if (warp >= 2) {
+    // The bf16 loads for all kRing K blocks of the ring are in flight at once
+    // (a register ring indexed at compile time), so DRAM latency is paid
+    // once, not once per block.  Ring position u holds K block kt0 + u, which
+    // belongs to stage slot u / kSuperK, block u % kSuperK.
+    if (warp >= 2 && warp < 2 + kQuantWarps) {
       constexpr int kRowsPerWarp = (BN + kQuantWarps - 1) / kQuantWarps;
       const int qw = warp - 2;
-      uint4 w[kStages][kRowsPerWarp];
-      auto load_tile = [&](int64_t kt, uint4 (&dst)[kRowsPerWarp]) {
+      uint4 w[kRing][kRowsPerWarp];
+      auto load_block = [&](int64_t kt, uint4 (&dst)[kRowsPerWarp]) {
         const int64_t col = kt * kTileK + lane * 8;
 #pragma unroll
         for (int i = 0; i < kRowsPerWarp; ++i) {
@@ -336,36 +338,39 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
         }
       };
 #pragma unroll
-      for (int u = 0; u < kStages; ++u) load_tile(kt_begin + u, w[u]);
-      uint32_t ph = 0;
+      for (int u = 0; u < kRing; ++u) load_block(kt_begin + u, w[u]);
       bool aborted = false;
-      for (int64_t kt0 = kt_begin; kt0 < kt_end && !aborted; kt0 += kStages) {
+      for (int64_t kt0 = kt_begin; kt0 < kt_end && !aborted; kt0 += kRing) {
+        const uint32_t round = (uint32_t)((kt0 - kt_begin) / kRing);
 #pragma unroll
-        for (int u = 0; u < kStages; ++u) {
+        for (int u = 0; u < kRing; ++u) {
           const int64_t kt = kt0 + u;
           if (kt >= kt_end || aborted) continue;
-          const bool slot_free = wait_bounded(&empty[u], ph ^ 1, abort_flag);
-          if (!__all_sync(0xFFFFFFFFu, slot_free)) {  // keep the warp's decision uniform
-            aborted = true;
-            continue;
+          const int s = u / kSuperK, j = u % kSuperK;
+          if (j == 0) {
+            const bool slot_free = wait_bounded(&empty[s], (round & 1) ^ 1, abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, slot_free)) {  // keep the warp's decision uniform
+              aborted = true;
+              continue;
+            }
           }
-          uint8_t* bd = smem + C::kOffBData + u * C::kBDataBytes;
-          uint8_t* bsf = smem + C::kOffBSf + u * C::kBSfBytes;
+          uint8_t* blk = smem + C::kOffB + s * C::kBBytes + j * C::kBBlock;
 #pragma unroll
           for (int i = 0; i < kRowsPerWarp; ++i) {
             const int row = qw + i * kQuantWarps;
             if (row < BN) {  // uniform across the warp
               uint32_t sbyte;
               const uint32_t packed = quantize_lane<kUseHardwareCvt>(w[u][i], sbyte);
-              *reinterpret_cast<uint32_t*>(bd + tile_data_offset(row, lane * 4)) = packed;
-              if ((lane & 3) == 0) bsf[tile_sf_offset(row, lane >> 2)] = (uint8_t)sbyte;
+              *reinterpret_cast<uint32_t*>(blk + tile_data_offset(row, lane * 4)) = packed;
+              if ((lane & 3) == 0) blk[C::kBSfOffset + tile_sf_offset(row, lane >> 2)] = (uint8_t)sbyte;
             }
           }
-          fence_proxy_async_smem();
-          mbar_arrive(&full[u]);
-          load_tile(kt + kStages, w[u]);  // refill this slot of the ring
+          if (j == kSuperK - 1 || kt == kt_end - 1) {  // stage complete
+            fence_proxy_async_smem();
+            mbar_arrive(&full[s]);
+          }
+          load_block(kt + kRing, w[u]);  // refill this ring position
         }
-        ph ^= 1;
       }
     }
   }
@@ -378,7 +383,7 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   float* red = reinterpret_cast<float*>(smem + C::kOffRed);
   __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem);
   const int rows_per_rank = kTileRows / split;
-  const int row_lo = rank * rows_per_rank, row_hi = row_lo + rows_per_rank;  // rows this CTA stores
+  const int row_lo = rank * rows_per_rank;  // first accumulator row this CTA stores
   __syncwarp();
   if (split > 1) cluster_wait();  // every rank's barriers are initialized
   if (warp >= 2 && warp < 6) {
@@ -511,6 +516,287 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   }
 }
 
+
+// ------------------------------------------------ persistent tile loop (m > 128, many tiles)
+// When the output has at least one 128 x 256 tile per SM, one CTA per SM
+// walks tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...  The bulk-copy
+// ring runs continuously across tiles, so the next tile's operands stream in
+// while the current tile's MMAs and epilogue run.
+//
+// Measured on GB300, this kernel's pipeline is shaped by three facts: the
+// bulk copies one thread issues are serialized (so each of the three operand
+// streams - activation rows, weight tile 0, weight tile 1 - has its own
+// issuing warp); a tcgen05.cp scale copy stalls the MMA queue for hundreds of
+// cycles (so four scale-factor warps write each row's e8m0 bytes into tensor
+// memory with tcgen05.st instead, one warp per 32-lane quadrant, and the MMA
+// thread issues nothing but MMAs); and a 128 x 128 x 64 block-scaled MMA
+// takes 64 cycles, so every 64-K step issues two N = 128 MMAs into the two
+// halves of the 128 x 256 accumulator.  The accumulator is handed back to the
+// MMA issuer once the epilogue warps have read it into registers
+// (acc_empty); their global stores overlap the next tile's MMAs.
+//
+// Warps: 0-3 epilogue, 4-7 scale factors, 8 activation copies (and setup),
+// 9 MMA issuer, 10-11 weight copies.
+struct PCfg {
+  static constexpr int BN = 256;
+  // ring depth and K blocks per stage: four single-block stages keep as many
+  // bytes in flight as two double-block ones but recycle slots twice as often
+  static constexpr int kStages = 4;
+  static constexpr int kSuperK = 1;
+  static constexpr int kThreads = 32 * 12;
+  static constexpr int kBTiles = 2;
+  static constexpr int kABytes = kSuperK * kTileBytes;
+  static constexpr int kBBytes = kBTiles * kSuperK * kTileBytes;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kStages * kABytes;
+  static constexpr int kOffStg = kOffB + kStages * kBBytes;
+  static constexpr int kStgPitch = 24;  // bf16 elements per staged row (16 + 8 pad)
+  static constexpr int kStgWarpBytes = 32 * kStgPitch * 2;
+  static constexpr int kOffBars = kOffStg + 4 * kStgWarpBytes;
+  static constexpr int kNumBars = 3 * kStages + 2;  // full, sf_full, empty per stage; acc_full, acc_empty
+  static constexpr int kOffMisc = kOffBars + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static constexpr int kSfColsPerBlock = 8 * (1 + kBTiles);  // per K block: A, B0, B1
+  static constexpr int kSfColsPerStage = kSuperK * kSfColsPerBlock;
+  static constexpr int kTmemCols = 512;
+  static_assert(BN + kStages * kSfColsPerStage <= kTmemCols, "tensor memory");
+  static constexpr int kWarpCopyA = 8, kWarpMma = 9, kWarpCopyB0 = 10;
+};
+
+__global__ void __launch_bounds__(PCfg::kThreads, 1)
+    gemm_persistent_kernel(const GemmArgs args, int64_t tiles_m, int64_t tiles_n) {
+  using P = PCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P::kOffBars);  // operand bytes landed
+  uint64_t* sf_full = full + P::kStages;                                 // scales written to tensor memory
+  uint64_t* empty = sf_full + P::kStages;                                // MMAs done with the stage
+  uint64_t* acc_full = empty + P::kStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t KT = args.kt_count;
+  const int64_t total = tiles_m * tiles_n;
+  const int nss = (int)ceil_div(KT, P::kSuperK);  // stages per tile
+  const int64_t b_row_tiles = ceil_div(args.b_rows, kTileRows);
+  auto stage_kblocks = [&](int ss) -> int {
+    const int64_t left = KT - (int64_t)ss * P::kSuperK;
+    return left < P::kSuperK ? (int)left : P::kSuperK;
+  };
+  // stream 0 = activation rows, streams 1, 2 = weight tiles; one issuing warp each
+  auto issue_stream = [&](int stream, int64_t tile, int ss, int s) {
+    const uint32_t bytes = (uint32_t)stage_kblocks(ss) * kTileBytes;
+    if (stream == 0) {
+      mbar_arrive_expect_tx(&full[s], bytes);
+      bulk_load(smem + P::kOffA + s * P::kABytes, args.a_img + image_block(tile % tiles_m, (int64_t)ss * P::kSuperK, KT),
+                bytes, &full[s]);
+    } else {
+      const int t = stream - 1;
+      const int64_t brt = (tile / tiles_m) * P::kBTiles + t;
+      if (brt >= b_row_tiles) {  // ragged last column tile: nothing to copy
+        mbar_arrive(&full[s]);
+        return;
+      }
+      mbar_arrive_expect_tx(&full[s], bytes);
+      bulk_load(smem + P::kOffB + s * P::kBBytes + t * P::kSuperK * kTileBytes,
+                args.b_img + image_block(brt, (int64_t)ss * P::kSuperK, KT), bytes, &full[s]);
+    }
+  };
+
+  if (threadIdx.x == P::kWarpCopyA * 32) {
+    for (int s = 0; s < P::kStages; ++s) {
+      mbar_init(&full[s], 3);     // one arrival per copy stream
+      mbar_init(&sf_full[s], 4);  // one arrival per scale-factor warp
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);  // one arrival per epilogue warp
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == P::kWarpMma) {
+    tmem_alloc(tmem_slot, P::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == P::kWarpCopyA || warp >= P::kWarpCopyB0) {
+    // ------------------------------------------------ bulk-copy producers
+    const int stream = warp == P::kWarpCopyA ? 0 : warp - P::kWarpCopyB0 + 1;
+    if (lane == 0 && blockIdx.x < total) {
+      // The activation image is written by the preceding kernel: its stream
+      // waits for that kernel; the weight streams start at once.
+      if (stream == 0) pdl_wait();
+      int64_t g = 0;  // stages issued so far
+      for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        bool stop = false;
+        for (int ss = 0; ss < nss; ++ss, ++g) {
+          const int s = (int)(g % P::kStages);
+          if (!wait_bounded(&empty[s], (uint32_t)(((g / P::kStages) & 1) ^ 1), abort_flag)) {
+            stop = true;
+            break;
+          }
+          issue_stream(stream, tile, ss, s);
+        }
+        if (stop) break;
+      }
+      if (*abort_flag) {  // let copies already in flight land before the CTA exits
+        for (int s = 0; s < P::kStages && s < g; ++s)
+          wait_bounded(&full[s], (uint32_t)(((g - 1 - s) / P::kStages) & 1), abort_flag, kDrainLimitCycles);
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------- scale factors into tensor memory
+    // The same column contents tcgen05.cp.32x128b.warpx4 would produce: lane
+    // l of every 32-lane quadrant holds the 16 bytes of atom row l in 4
+    // columns (row groups l, l+32, l+64, l+96; K blocks 0-3), then the 16
+    // bytes of the second atom (K blocks 4-7) in the next 4 columns.  Warp q
+    // writes quadrant q, 8 columns per operand and K block.
+    const int quad = warp - 4;
+    int64_t g = 0;
+    for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      bool stop = false;
+      for (int ss = 0; ss < nss; ++ss, ++g) {
+        const int s = (int)(g % P::kStages);
+        if (!__all_sync(0xFFFFFFFFu, wait_bounded(&full[s], (uint32_t)((g / P::kStages) & 1), abort_flag))) {
+          stop = true;
+          break;
+        }
+        const int cnt = stage_kblocks(ss);
+        for (int j = 0; j < P::kSuperK; ++j) {
+          if (j >= cnt) break;
+          const uint8_t* sf_src[3] = {smem + P::kOffA + s * P::kABytes + j * kTileBytes + kTileDataBytes,
+                                      smem + P::kOffB + s * P::kBBytes + j * kTileBytes + kTileDataBytes,
+                                      smem + P::kOffB + s * P::kBBytes + (P::kSuperK + j) * kTileBytes + kTileDataBytes};
+#pragma unroll
+          for (int o = 0; o < 3; ++o) {
+            const uint4 lo = *reinterpret_cast<const uint4*>(sf_src[o] + lane * 16);
+            const uint4 hi = *reinterpret_cast<const uint4*>(sf_src[o] + kAtomBytes + lane * 16);
+            const uint32_t v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+            const uint32_t col = P::BN + s * P::kSfColsPerStage + j * P::kSfColsPerBlock + o * 8;
+            tmem_store_8(tmem + ((uint32_t)(quad * 32) << 16) + col, v);
+          }
+        }
+        tmem_store_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_full[s]);
+      }
+      if (stop) break;
+    }
+  } else if (warp == P::kWarpMma) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int64_t g = 0;
+      uint32_t it = 0;
+      for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+        if (!wait_bounded(acc_empty, (it & 1) ^ 1, abort_flag)) break;  // previous tile drained
+        tc_fence_after();
+        bool aborted = false;
+        bool accumulate = false;
+        for (int ss = 0; ss < nss; ++ss, ++g) {
+          const int s = (int)(g % P::kStages);
+          const uint32_t ph = (uint32_t)((g / P::kStages) & 1);
+          if (!wait_bounded(&full[s], ph, abort_flag) || !wait_bounded(&sf_full[s], ph, abort_flag)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const int cnt = stage_kblocks(ss);
+          for (int j = 0; j < cnt; ++j) {
+            const uint32_t a_blk = smem_addr(smem + P::kOffA + s * P::kABytes + j * kTileBytes);
+            const uint32_t b0 = smem_addr(smem + P::kOffB + s * P::kBBytes + j * kTileBytes);
+            const uint32_t b1 = b0 + P::kSuperK * kTileBytes;
+            const uint32_t sf = tmem + P::BN + s * P::kSfColsPerStage + j * P::kSfColsPerBlock;
+            const uint64_t ad = smem_desc(a_blk, 0, 1024, kLayoutSwizzle128);
+            const uint64_t bd0 = smem_desc(b0, 0, 1024, kLayoutSwizzle128);
+            const uint64_t bd1 = smem_desc(b1, 0, 1024, kLayoutSwizzle128);
+            const int steps = k_steps(args.k, (int64_t)ss * P::kSuperK + j);
+            for (int kk = 0; kk < steps; ++kk) {
+              // advancing the start address by 32 bytes = 2 in the descriptor's 16-byte units
+              const uint64_t adv = (uint64_t)(kk * 2);
+              const uint32_t id = (uint32_t)(kk & 1) * 2;
+              const uint32_t acc = accumulate ? 1u : 0u;
+              const uint32_t sfk = (uint32_t)(kk >> 1) * 4;
+              mma_mxf4(tmem, ad + adv, bd0 + adv, idesc_mxf4(128, 128, id, id), sf + sfk, sf + 8 + sfk, acc);
+              mma_mxf4(tmem + 128, ad + adv, bd1 + adv, idesc_mxf4(128, 128, id, id), sf + sfk, sf + 16 + sfk, acc);
+              accumulate = true;
+            }
+          }
+          mma_commit(&empty[s]);
+        }
+        mma_commit(acc_full);  // fires when this tile's MMAs have completed
+        if (aborted) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // --------------------------------------------- epilogue (warps 0-3)
+    // The whole 32 x 256 slice of the accumulator is read into registers as
+    // packed bf16 (128 registers) before the accumulator is handed back, so
+    // the next tile's MMAs wait only for the tensor-memory reads, not for
+    // the global stores.
+    const int quad = warp;
+    __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem + P::kOffStg + warp * P::kStgWarpBytes);
+    uint32_t it = 0;
+    for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+      const int64_t m0 = (tile % tiles_m) * kTileRows + quad * 32;
+      const int64_t n0 = (tile / tiles_m) * P::BN;
+      const bool ok = wait_bounded(acc_full, it & 1, abort_flag);
+      tc_fence_after();
+      uint32_t packed[P::BN / 16][8];
+#pragma unroll
+      for (int c = 0; c < P::BN / 16; ++c) {
+        uint32_t r[16];
+        tmem_load_16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(c * 16), r);
+        tmem_load_wait();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) packed[c][j] = bf16x2_bits(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);  // accumulator free for the next tile
+      if (!ok) continue;
+#pragma unroll
+      for (int c = 0; c < P::BN / 16; ++c) {
+        uint4* row_dst = reinterpret_cast<uint4*>(stg + lane * P::kStgPitch);
+        row_dst[0] = make_uint4(packed[c][0], packed[c][1], packed[c][2], packed[c][3]);
+        row_dst[1] = make_uint4(packed[c][4], packed[c][5], packed[c][6], packed[c][7]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int row = i * 16 + (lane >> 1), ch = lane & 1;
+          const int64_t mi = m0 + row;
+          const int64_t n = n0 + c * 16 + ch * 8;
+          if (mi < args.m && n < args.n) {
+            const __nv_bfloat16* src = stg + row * P::kStgPitch + ch * 8;
+            __nv_bfloat16* dst = args.c + mi * args.ldc + n;
+            if (n + 8 <= args.n) {
+              *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+            } else {
+              for (int e = 0; e < 8 && n + e < args.n; ++e) dst[e] = src[e];
+            }
+          }
+        }
+        __syncwarp();  // the next chunk reuses the staging slice
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == P::kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, P::kTmemCols);
+  }
+}
+
 // ------------------------------------------------------------------ host
 int num_sms() {
   static int cached[64] = {0};
@@ -564,6 +850,11 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan) {
     p.split = s;
     p.grid_y = nt * s;
     p.workspace = (size_t)image_bytes(m, k);
+    if (p.bn == 256) {  // at least one 128 x 256 tile per SM: persistent tile loop
+      p.persistent = true;
+      p.grid_x = mt * nt < sms ? mt * nt : sms;
+      p.grid_y = 1;
+    }
   }
   if (p.grid_x > 0x7FFFFFFF || p.grid_y > 65535) return 1;
   *plan = p;
@@ -607,6 +898,30 @@ static cudaError_t launch_one(const GemmPlan& plan, const GemmArgs& args, cudaSt
   return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, kMode>, args);
 }
 
+static cudaError_t launch_persistent(const GemmPlan& plan, const GemmArgs& args, int64_t tiles_m, int64_t tiles_n,
+                                     cudaStream_t stream) {
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)plan.grid_x, 1, 1);
+  cfg.blockDim = dim3(PCfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = PCfg::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;  // dependent of the quantization kernel
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_persistent_kernel, args, tiles_m, tiles_n);
+}
+
 cudaError_t launch_gemm(const GemmPlan& plan, const void* a_bf16, int64_t m, int64_t k, int64_t lda,
                         const void* b_image, int64_t n, void* c, int64_t ldc, void* workspace,
                         cudaStream_t stream) {
@@ -621,7 +936,6 @@ cudaError_t launch_gemm(const GemmPlan& plan, const void* a_bf16, int64_t m, int
   args.lda = lda;
   if (plan.mode == kFusedSwap) {
     args.a_img = static_cast<const uint8_t*>(b_image);
-    args.a_rows = n;
     args.act = static_cast<const uint16_t*>(a_bf16);
     switch (plan.bn) {
       case 16: return launch_one<16, kFusedSwap>(plan, args, stream);
@@ -633,7 +947,6 @@ cudaError_t launch_gemm(const GemmPlan& plan, const void* a_bf16, int64_t m, int
   if (e != cudaSuccess) return e;
   if (plan.mode == kImageSwap) {
     args.a_img = static_cast<const uint8_t*>(b_image);
-    args.a_rows = n;
     args.b_img = static_cast<const uint8_t*>(workspace);
     args.b_rows = m;
     switch (plan.bn) {
@@ -643,12 +956,11 @@ cudaError_t launch_gemm(const GemmPlan& plan, const void* a_bf16, int64_t m, int
     }
   }
   args.a_img = static_cast<const uint8_t*>(workspace);
-  args.a_rows = m;
   args.b_img = static_cast<const uint8_t*>(b_image);
   args.b_rows = n;
+  if (plan.persistent) return launch_persistent(plan, args, ceil_div(m, kTileRows), ceil_div(n, PCfg::BN), stream);
   switch (plan.bn) {
     case 128: return launch_one<128, kImagePlain>(plan, args, stream);
-    case 256: return launch_one<256, kImagePlain>(plan, args, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -67,7 +67,6 @@ __global__ void __launch_bounds__(kQuantThreads)
   const int64_t total = m * kt_count;
   const int64_t nwarps = (int64_t)gridDim.x * (kQuantThreads / 32);
   const int64_t warp0 = (int64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
-  uint8_t* sf_region = img + image_sf_region(m, k);
   for (int64_t base = warp0; base < total; base += nwarps * kQuantUnroll) {
     uint4 w[kQuantUnroll];
     int64_t row[kQuantUnroll], kt[kQuantUnroll];
@@ -88,9 +87,9 @@ __global__ void __launch_bounds__(kQuantThreads)
       const uint32_t packed = quantize_lane<kHw>(w[u], sbyte);
       if (live[u]) {
         const int r = (int)(row[u] & (kTileRows - 1));
-        const int64_t tile = (row[u] / kTileRows) * kt_count + kt[u];
-        *reinterpret_cast<uint32_t*>(img + tile * kTileDataBytes + tile_data_offset(r, lane * 4)) = packed;
-        if ((lane & 3) == 0) sf_region[tile * kTileSfBytes + tile_sf_offset(r, lane >> 2)] = (uint8_t)sbyte;
+        uint8_t* blk = img + image_block(row[u] / kTileRows, kt[u], kt_count);
+        *reinterpret_cast<uint32_t*>(blk + tile_data_offset(r, lane * 4)) = packed;
+        if ((lane & 3) == 0) blk[kTileDataBytes + tile_sf_offset(r, lane >> 2)] = (uint8_t)sbyte;
       }
     }
   }
@@ -111,7 +110,7 @@ __global__ void __launch_bounds__(256)
     const int64_t kbyte = (tile % kt_count) * (kTileK / 2) + c * 16;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (row < n && kbyte < k / 2) v = *reinterpret_cast<const uint4*>(bq + row * (k / 2) + kbyte);
-    *reinterpret_cast<uint4*>(img + tile * kTileDataBytes + tile_data_offset(r, c * 16)) = v;
+    *reinterpret_cast<uint4*>(img + tile * kTileBytes + tile_data_offset(r, c * 16)) = v;
   }
 }
 
@@ -119,7 +118,6 @@ __global__ void __launch_bounds__(256)
     prepack_scale_kernel(const uint8_t* __restrict__ bs, int64_t n, int64_t k, uint8_t* __restrict__ img) {
   const int64_t kt_count = ceil_div(k, kTileK);
   const int64_t total = ceil_div(n, kTileRows) * kt_count * kTileSfBytes;
-  uint8_t* sf_region = img + image_sf_region(n, k);
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int64_t tile = idx / kTileSfBytes;
@@ -129,7 +127,7 @@ __global__ void __launch_bounds__(256)
     const int64_t blk = (tile % kt_count) * (kTileK / 32) + b;
     uint8_t v = 0;
     if (row < n && blk < k / 32) v = bs[row * (k / 32) + blk];
-    sf_region[tile * kTileSfBytes + tile_sf_offset(r, b)] = v;
+    img[tile * kTileBytes + kTileDataBytes + tile_sf_offset(r, b)] = v;
   }
 }
 

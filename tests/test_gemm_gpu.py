@@ -178,3 +178,17 @@ def test_gemm_every_split_factor(m, n, k, split, monkeypatch):
     c2 = mx.gemm(a_dev, packed, out=torch.empty((m, ldc), dtype=torch.bfloat16, device="cuda")[:, :n])
     torch.cuda.synchronize()
     assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+
+
+def test_persistent_tile_loop_with_ragged_tails():
+    """m=1000, n=4856, k=544: 8 x 19 = 152 output tiles of 128 x 256 (at least one
+    per SM) run through the persistent tile loop; the last row tile, the last
+    column tile (248 of 256 columns, the second weight tile partial) and the
+    last K tile (32 of 256) are all ragged, and some CTAs take two tiles."""
+    m, n, k = 1000, 4856, 544
+    a = inputs.random_bf16(m, k, seed=77)
+    b = inputs.random_bf16(n, k, seed=78, std=0.2)
+    packed, bq, bs = packed_from_oracle(b)
+    got, c_full = _run(a, packed, ldc=n + 8)
+    assert_close_to_ref(got, _oracle_full(a, bq, bs), what="persistent")
+    assert torch.isnan(c_full[:, n:]).all()
