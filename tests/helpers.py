@@ -47,3 +47,21 @@ def packed_from_oracle(b_bf16: torch.Tensor, device="cuda"):
     bq, bs = oracle_weights(b_bf16)
     packed = mx.prepack_b(torch.from_numpy(bq).to(device), torch.from_numpy(bs).to(device))
     return packed, bq, bs
+
+
+def gloo_max_over_ranks_worker(rank: int, world: int, port: int, values, out_queue):
+    """Child of the 2-rank gloo test: bench.py's barrier and max-over-ranks."""
+    import os
+    import torch.distributed as dist
+
+    import bench
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.barrier(world)
+        got = bench.max_over_ranks(values[rank], world)
+        bench.barrier(world)
+        out_queue.put((rank, got))
+    finally:
+        dist.destroy_process_group()

@@ -1,0 +1,40 @@
+"""Failure detection without a GPU fault: every pipeline wait in the GEMM is
+bounded.  With MXFP4_DEBUG_DROP_COPIES=1 the kernel issues no bulk copies, so
+the MMA issuer's wait for its first stage runs out (about a second); the
+kernel raises the device-side timeout flag and returns normally.  The host
+reads MXFP4_ERR_TIMEOUT from mxfp4_device_status, and the context stays
+usable: the next call computes the right result."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import precision_bf16_mxfp4_gb300 as mx
+from precision_bf16_mxfp4_gb300 import _lib, inputs
+from tests.helpers import assert_close_to_ref, packed_from_oracle
+import oracle
+from tests.helpers import bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("m,split", [(8, "1"), (16, "4"), (48, "2")])
+def test_wait_timeout_is_reported_and_recoverable(m, split, monkeypatch):
+    n, k = 256, 1024
+    a = inputs.random_bf16(m, k, seed=m)
+    b = inputs.random_bf16(n, k, seed=n, std=0.3)
+    packed, bq, bs = packed_from_oracle(b)
+    a_dev = a.cuda()
+    monkeypatch.setenv("MXFP4_SPLIT_K", split)
+    monkeypatch.setenv("MXFP4_DEBUG_DROP_COPIES", "1")
+    mx.gemm(a_dev, packed)
+    with pytest.raises(mx.Mxfp4Error) as e:
+        mx.device_status()
+    assert e.value.status == _lib.MXFP4_ERR_TIMEOUT
+    monkeypatch.delenv("MXFP4_DEBUG_DROP_COPIES")
+    mx.device_status()  # the flag was cleared by the previous read
+    c = mx.gemm(a_dev, packed)
+    mx.device_status()
+    aq, a_s = oracle.quant(bf16_bits(a))
+    assert_close_to_ref(c.float().cpu().numpy(), oracle.gemm_via_dequant(aq, a_s, bq, bs))
