@@ -80,10 +80,12 @@ template <int BN, int kMode>
 struct Cfg {
   static constexpr bool kFused = kMode == kFusedSwap;
   static constexpr bool kSwap = kMode != kImagePlain;
-  // warps: 0 and the last one issue bulk copies (even / odd stages), 1 issues
-  // MMAs, 2-5 drain the accumulator, 2-7 quantize A in kFusedSwap
-  static constexpr int kThreads = kFused ? 32 * (3 + kQuantWarps) : 32 * 7;
-  static constexpr int kOddProducerWarp = kThreads / 32 - 1;
+  // warps: 0 issues bulk copies (in the image modes the last warp issues the
+  // odd stages after the first round), 1 issues MMAs, 2-5 drain the
+  // accumulator, 2-7 quantize A in kFusedSwap (whose few stages warp 0 issues
+  // alone: a smaller CTA lets more split-K clusters be resident)
+  static constexpr int kThreads = kFused ? 32 * (2 + kQuantWarps) : 32 * 7;
+  static constexpr int kOddProducerWarp = kFused ? 0 : kThreads / 32 - 1;
   static constexpr int kBRows = BN;                                    // MMA N (<= 128 here)
   static constexpr int kABytes = kSuperK * kTileBytes;                 // MMA-A bytes per stage
   static constexpr int kBBlock = kFused ? BN * 128 + kTileSfBytes : kTileBytes;  // per K block
@@ -221,9 +223,8 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
 
   if (threadIdx.x == 0) {
     // The weight stream is the long pole: initialize the barriers and start
-    // stage 0 at once; the odd-stage producer starts stage 1 after the
-    // prologue barrier.  The operand the preceding kernel writes is requested
-    // only after the dependency wait.
+    // the first round of stages at once.  The operand the preceding kernel
+    // writes is requested only after the dependency wait.
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1 + (C::kFused ? kQuantWarps * 32 : 0));
       mbar_init(&empty[s], 1);
@@ -233,15 +234,20 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     mbar_init(red_full, (uint32_t)((split > 1 ? split - 1 : 1) * (split > 4 ? 1 : 4 / split)));
     *abort_flag = 0;
     fence_mbar_init();
-    if (nss > 0 && !args.drop_copies) {
+    if (!args.drop_copies) {
       const uint64_t pol_weights = policy_evict_first(), pol_act = policy_evict_last();
-      mbar_arrive_expect_tx(&full[0], stage_bytes(0));
-      if (!kADependent) issue_a(0, 0, kMode == kImagePlain ? pol_act : pol_weights);
-      if (!C::kFused && !kBDependent) issue_b(0, 0, pol_weights);
+      const int pre = nss < kStages ? nss : kStages;
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], stage_bytes(i));
+        if (!kADependent) issue_a(i, i, kMode == kImagePlain ? pol_act : pol_weights);
+        if (!C::kFused && !kBDependent) issue_b(i, i, pol_weights);
+      }
       if (kADependent || kBDependent) {
         pdl_wait();
-        if (kADependent) issue_a(0, 0, pol_act);
-        if (kBDependent) issue_b(0, 0, pol_act);
+        for (int i = 0; i < pre; ++i) {
+          if (kADependent) issue_a(i, i, pol_act);
+          if (kBDependent) issue_b(i, i, pol_act);
+        }
       }
     }
   }
@@ -262,12 +268,13 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     // two slots' copies are issued by two warps and move concurrently.
     if (lane == 0) {
       const int slot = warp == 0 ? 0 : 1;
+      const int stride = C::kOddProducerWarp == 0 ? 1 : kStages;  // one producer covers every stage
       const uint64_t pol_weights = policy_evict_first(), pol_act = policy_evict_last();
       const uint64_t pol_a = kMode == kImagePlain ? pol_act : pol_weights;
       const uint64_t pol_b = kMode == kImageSwap ? pol_act : pol_weights;
-      bool waited_dependency = slot == 0;  // thread 0 already waited in the prologue
-      for (int ss = slot; ss < nss && !args.drop_copies; ss += kStages) {
-        if (ss == 0) continue;  // issued in the prologue
+      bool waited_dependency = false;
+      for (int ss = slot; ss < nss && !args.drop_copies; ss += stride) {
+        if (ss < kStages) continue;  // issued in the prologue
         const int s = ss % kStages;
         if (!wait_bounded(&empty[s], (uint32_t)(((ss / kStages) & 1) ^ 1), abort_flag)) break;
         mbar_arrive_expect_tx(&full[s], stage_bytes(ss));
@@ -282,9 +289,11 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
           if (kBDependent) issue_b(ss, s, pol_b);
         }
       }
-      if (*abort_flag && slot < nss) {  // let this slot's copies in flight land before the CTA exits
-        const int last = slot + ((nss - 1 - slot) / kStages) * kStages;
-        wait_bounded(&full[slot], (uint32_t)((last / kStages) & 1), abort_flag, kDrainLimitCycles);
+      if (*abort_flag) {  // let the copies in flight land before the CTA exits
+        for (int t = slot; t < kStages && t < nss; t += stride) {
+          const int last = t + ((nss - 1 - t) / kStages) * kStages;
+          wait_bounded(&full[t], (uint32_t)((last / kStages) & 1), abort_flag, kDrainLimitCycles);
+        }
       }
     }
   } else if (warp == 1) {
@@ -846,7 +855,7 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan) {
     const int64_t nt = ceil_div(n, p.bn);
     const int s_max = p.bn == 256 ? 1 : 8;  // the kernels' kMaxSplit
     int s = 1;
-    while (s < s_max && mt * nt * s * 2 <= sms && KT / (s * 2) >= 2) s *= 2;
+    while (s < s_max && mt * nt * s * 2 <= sms && KT / (s * 2) >= 4) s *= 2;
     if (forced) s = (forced <= KT && forced <= s_max) ? forced : 1;
     p.split = s;
     p.grid_y = nt * s;
@@ -862,10 +871,42 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan) {
   return 0;
 }
 
+// Thread-block clusters of a given size that can be resident at once for this
+// kernel (cached per device and cluster size).
 template <int BN, int kMode>
-static cudaError_t launch_one(const GemmPlan& plan, const GemmArgs& args, cudaStream_t stream) {
+static int max_resident_clusters(int split) {
   using C = Cfg<BN, kMode>;
-  if (plan.split > C::kMaxSplit) return cudaErrorInvalidConfiguration;
+  static int cache[64][4] = {};  // [device][log2 split - 1]
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int idx = split == 2 ? 0 : split == 4 ? 1 : split == 8 ? 2 : 3;
+  if (dev < 0 || dev >= 64) return 0;
+  if (cache[dev][idx] == 0) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(1, (unsigned)split, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 1;
+    attr.val.clusterDim.y = (unsigned)split;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<BN, kMode>, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();  // clear the error: the launch decides
+      n = -1;
+    }
+    cache[dev][idx] = n;
+  }
+  return cache[dev][idx];
+}
+
+template <int BN, int kMode>
+static cudaError_t launch_one(const GemmPlan& plan_in, const GemmArgs& args_in, cudaStream_t stream) {
+  using C = Cfg<BN, kMode>;
+  if (plan_in.split > C::kMaxSplit) return cudaErrorInvalidConfiguration;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -875,6 +916,17 @@ static cudaError_t launch_one(const GemmPlan& plan, const GemmArgs& args, cudaSt
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
+  // A K split whose clusters cannot all be resident at once would run in two
+  // waves; halve it until they fit (the result does not depend on the split).
+  GemmPlan plan = plan_in;
+  GemmArgs args = args_in;
+  while (plan.split > 1) {
+    const int fit = max_resident_clusters<BN, kMode>(plan.split);
+    if (fit < 0 || (int64_t)fit * plan.split >= plan.grid_x * plan.grid_y) break;
+    plan.grid_y = plan.grid_y / plan.split * (plan.split / 2);
+    plan.split /= 2;
+  }
+  args.split = plan.split;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)plan.grid_x, (unsigned)plan.grid_y, 1);
   cfg.blockDim = dim3(C::kThreads, 1, 1);
