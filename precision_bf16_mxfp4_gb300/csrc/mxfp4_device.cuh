@@ -54,12 +54,15 @@ __host__ __device__ inline int tile_sf_offset(int r, int b) {
 }
 
 // ------------------------------------------------------------ quantization
-// Largest |x| among 8 bf16 values, as a 15-bit magnitude pattern (for finite
-// values the pattern order is the magnitude order).
-__device__ __forceinline__ uint32_t absmax8_bits(const uint4& w) {
-  uint32_t a = __vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu);
-  uint32_t b = __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu);
-  uint32_t c = __vmaxu2(a, b);
+// Largest |x| among the 32 bf16 values of one block, as a 15-bit magnitude
+// pattern (for finite values the pattern order is the magnitude order).
+__device__ __forceinline__ uint32_t absmax32_bits(const uint4 (&w)[4]) {
+  constexpr uint32_t kMag = 0x7FFF7FFFu;
+  uint32_t p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    p[i] = __vmaxu2(__vmaxu2(w[i].x & kMag, w[i].y & kMag), __vmaxu2(w[i].z & kMag, w[i].w & kMag));
+  const uint32_t c = __vmaxu2(__vmaxu2(p[0], p[1]), __vmaxu2(p[2], p[3]));
   return max(c & 0xFFFFu, c >> 16);
 }
 
@@ -118,17 +121,16 @@ __device__ __forceinline__ uint32_t encode8(const uint4& w, float inv_scale) {
   return out;
 }
 
-// One lane's share of a 32-element block: 8 elements (16 bytes of bf16).
-// Lanes 4j..4j+3 of a warp hold block j; the block maximum is formed with two
-// butterfly shuffles.  Returns the packed 4 bytes; `scale_byte` gets e8m0.
+// One 32-element block (64 bytes of bf16 in K order) -> 16 bytes of packed
+// e2m1 (byte i holds elements 2i and 2i+1) and its e8m0 scale byte.  One
+// thread owns the whole block, so the block maximum needs no shuffles.
 template <bool kHardwareCvt>
-__device__ __forceinline__ uint32_t quantize_lane(const uint4& w, uint32_t& scale_byte) {
-  uint32_t amax = absmax8_bits(w);
-  amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-  amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-  const int ub = block_exponent(amax);
+__device__ __forceinline__ uint4 quantize_block32(const uint4 (&w)[4], uint32_t& scale_byte) {
+  const int ub = block_exponent(absmax32_bits(w));
   scale_byte = (uint32_t)(ub + 127);
-  return encode8<kHardwareCvt>(w, inverse_scale(ub));
+  const float inv = inverse_scale(ub);
+  return make_uint4(encode8<kHardwareCvt>(w[0], inv), encode8<kHardwareCvt>(w[1], inv),
+                    encode8<kHardwareCvt>(w[2], inv), encode8<kHardwareCvt>(w[3], inv));
 }
 
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
@@ -137,6 +139,12 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
+}
+
+// The 64 bytes of one 32-element block from global memory (read-only path).
+__device__ __forceinline__ void ldg_nc_block(const uint16_t* p, uint4 (&w)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w[i] = ldg_nc_v4(p + 8 * i);
 }
 
 }  // namespace mxfp4

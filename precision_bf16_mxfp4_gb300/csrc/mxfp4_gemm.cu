@@ -35,8 +35,9 @@
 // slots in rank order (deterministic) and stores its rows.
 //
 // Warp roles: warp 0 issues bulk copies; warp 1 owns tensor memory and issues
-// scale-factor copies and MMAs (one thread); warps 2-5 drain the accumulator;
-// in kFusedSwap warps 2-7 quantize the activations.  Every wait is bounded: a
+// the MMAs (one thread); warps 2-5 write each stage's scale factors into
+// tensor memory (tcgen05.st) and drain the accumulator; in kFusedSwap warps
+// 2 .. 1 + BN/4 quantize the activations.  Every wait is bounded: a
 // wait that runs out sets a device flag and the CTA winds down.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -57,7 +58,6 @@ constexpr long long kWaitLimitCycles = 1ll << 31;
 constexpr long long kDrainLimitCycles = 1ll << 25;  // ~20 ms when winding down after a timeout
 constexpr int kSuperK = 2;                          // K blocks per pipeline stage
 constexpr int kStages = 2;                          // stages in the ring
-constexpr int kQuantWarps = 6;
 constexpr int kRing = kSuperK * kStages;            // K blocks in flight
 
 enum GemmMode : int { kFusedSwap = 0, kImageSwap = 1, kImagePlain = 2 };
@@ -81,9 +81,13 @@ struct Cfg {
   static constexpr bool kFused = kMode == kFusedSwap;
   static constexpr bool kSwap = kMode != kImagePlain;
   // warps: 0 issues bulk copies (in the image modes the last warp issues the
-  // odd stages after the first round), 1 issues MMAs, 2-5 drain the
-  // accumulator, 2-7 quantize A in kFusedSwap (whose few stages warp 0 issues
-  // alone: a smaller CTA lets more split-K clusters be resident)
+  // odd stages after the first round), 1 issues MMAs, 2-5 write the scale
+  // factors to tensor memory and drain the accumulator; in kFusedSwap warps
+  // 2 .. 2 + BN/4 - 1 quantize A, one thread per row and 32-element block of
+  // a K block (BN rows x 8 blocks), and warp 0 issues the few stages alone
+  static constexpr int kQuantWarps = kFused ? BN / 4 : 0;
+  static constexpr int kEpiWarps = kQuantWarps >= 8 ? 8 : 4;  // accumulator-draining warps (from warp 2)
+  static constexpr int kEpiCols = BN / (kEpiWarps / 4);         // accumulator columns per draining warp
   static constexpr int kThreads = kFused ? 32 * (2 + kQuantWarps) : 32 * 7;
   static constexpr int kOddProducerWarp = kFused ? 0 : kThreads / 32 - 1;
   static constexpr int kBRows = BN;                                    // MMA N (<= 128 here)
@@ -94,7 +98,7 @@ struct Cfg {
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
   static constexpr int kOffBars = kOffB + kStages * kBBytes;
-  static constexpr int kOffMisc = kOffBars + (2 * kStages + 2) * 8;
+  static constexpr int kOffMisc = kOffBars + (4 * kStages + 2) * 8;
   // split-K partials of the rows this rank owns land in a region of their own:
   // another rank may push while this CTA's MMAs still read the stage buffers
   static constexpr int kMaxSplit = 8;
@@ -103,8 +107,8 @@ struct Cfg {
   static constexpr int kOffRed = (kOffMisc + 16 + 15) & ~15;
   static constexpr int kSmemBytes = kOffRed + kRedBytes + 1024;  // + alignment slack
   // bf16 output staging reuses the stage buffers once the accumulator is complete
-  static constexpr int kStgPitch = kSwap ? 128 : BN + 8;  // elements
-  static constexpr int kStgBytes = (kSwap ? BN : 128) * kStgPitch * 2;
+  static constexpr int kStgPitch = BN + 8;  // elements (kImagePlain)
+  static constexpr int kStgBytes = kSwap ? 0 : 128 * kStgPitch * 2;
   static_assert(kStgBytes <= kOffBars, "output staging must fit in the stage buffers");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(kBBlock % 1024 == 0, "swizzled operand blocks must stay 1024-byte aligned");
@@ -169,6 +173,20 @@ __device__ __forceinline__ void copy_block_scales(uint32_t tmem_col, uint32_t sf
   tmem_copy_32x128b_x4(tmem_col + 4, smem_desc(sf_smem + kAtomBytes, 0, 128, kLayoutNoSwizzle));
 }
 
+// Scale factors of one K block (two 512-byte atoms in shared memory) into 8
+// tensor-memory columns of the calling warp's 32-lane quadrant, with the
+// column contents tcgen05.cp.32x128b.warpx4 would produce: lane l holds the
+// 16 bytes of atom row l (row groups l, l+32, l+64, l+96; K blocks 0-3) in 4
+// columns and the second atom's 16 bytes (K blocks 4-7) in the next 4.
+// Measured on GB300, a tcgen05.cp stalls the MMA queue for hundreds of
+// cycles; these stores run on the warps that have nothing else to do.
+__device__ __forceinline__ void store_block_scales(uint32_t taddr, const uint8_t* sf_smem, int lane) {
+  const uint4 lo = *reinterpret_cast<const uint4*>(sf_smem + lane * 16);
+  const uint4 hi = *reinterpret_cast<const uint4*>(sf_smem + kAtomBytes + lane * 16);
+  const uint32_t v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  tmem_store_8(taddr, v);
+}
+
 // K steps of 64 in the K block starting at element kt * 256
 __device__ __forceinline__ int k_steps(int64_t k, int64_t kt) {
   const int64_t rem = k - kt * kTileK;
@@ -184,6 +202,8 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   uint64_t* empty = full + kStages;
   uint64_t* accum = empty + kStages;
   uint64_t* red_full = accum + 1;  // the other ranks' partial rows owned by this rank have landed
+  uint64_t* act_ready = red_full + 1;      // kFusedSwap: the stage's activations are quantized
+  uint64_t* sf_ready = act_ready + kStages;  // the stage's scale factors are in tensor memory
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -196,6 +216,30 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   const int64_t kt_begin = KT * rank / split;
   const int64_t kt_end = KT * (rank + 1) / split;
   const int nss = (int)ceil_div(kt_end - kt_begin, kSuperK);  // pipeline stages this CTA runs
+
+  // kFusedSwap: the quantizer threads start loading their bf16 blocks for
+  // the first kRing K blocks right away, before any setup: DRAM latency is
+  // the long pole.  Ring position u holds K block kt0 + u (stage slot
+  // u / kSuperK, block u % kSuperK); the register ring is indexed at compile
+  // time.  Quantizer thread qt owns row qt / 8 and 32-element block qt % 8 of
+  // every K block.
+  const bool quantizer = C::kFused && warp >= 2 && warp < 2 + C::kQuantWarps;
+  const int qt = (int)threadIdx.x - 64;
+  const int q_row = qt >> 3, q_blk = qt & 7;
+  uint4 w[kRing][4];
+  auto load_block = [&](int64_t kt, uint4 (&dst)[4]) {
+    const int64_t col = kt * kTileK + q_blk * 32;
+    if (kt < kt_end && q_row < args.m && col < args.k) {
+      ldg_nc_block(args.act + q_row * args.lda + col, dst);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+    }
+  };
+  if (quantizer) {
+#pragma unroll
+    for (int u = 0; u < kRing; ++u) load_block(kt_begin + u, w[u]);
+  }
 
   // operand written by the preceding quantization kernel
   constexpr bool kADependent = kMode == kImagePlain;
@@ -226,12 +270,14 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     // the first round of stages at once.  The operand the preceding kernel
     // writes is requested only after the dependency wait.
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1 + (C::kFused ? kQuantWarps * 32 : 0));
+      mbar_init(&full[s], 1);                   // the bulk copies' bytes
+      if (C::kFused) mbar_init(&act_ready[s], C::kQuantWarps * 32);  // every quantizer thread
+      mbar_init(&sf_ready[s], 4);               // one arrival per scale-factor warp
       mbar_init(&empty[s], 1);
     }
     mbar_init(accum, 1);
     // one arrival per (other rank, warp holding some of this rank's rows)
-    mbar_init(red_full, (uint32_t)((split > 1 ? split - 1 : 1) * (split > 4 ? 1 : 4 / split)));
+    mbar_init(red_full, (uint32_t)((split > 1 ? split - 1 : 1) * (split > 4 ? 1 : 4 / split) * (C::kEpiWarps / 4)));
     *abort_flag = 0;
     fence_mbar_init();
     if (!args.drop_copies) {
@@ -252,6 +298,14 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     }
   }
   if (warp == 1) {
+    if (lane < 2) {  // first and last C row of this CTA's output tile
+      const int64_t r0 = C::kSwap ? 0 : a_tile * kTileRows;
+      const int64_t rows = C::kSwap ? args.m : args.m - r0;
+      const int64_t r = r0 + (lane == 0 ? 0 : (rows < kTileRows ? rows : kTileRows) - 1);
+      const int64_t col = C::kSwap ? a_tile * kTileRows : b_tile * BN;
+      if (r < args.m && col < args.n) prefetch_l1(args.c + r * args.ldc + col);
+    }
+    __syncwarp();
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
@@ -302,23 +356,37 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
       bool accumulate = false;
       for (int ss = 0; ss < nss; ++ss) {
         const int s = ss % kStages;
-        if (!wait_bounded(&full[s], (uint32_t)((ss / kStages) & 1), abort_flag)) break;
+        const uint32_t ph = (uint32_t)((ss / kStages) & 1);
+        if (!wait_bounded(&full[s], ph, abort_flag) || !wait_bounded(&sf_ready[s], ph, abort_flag)) break;
         tc_fence_after();
         const uint32_t sfa = tmem + C::kAccCols + s * C::kSfColsPerStage;
         const uint32_t sfb = sfa + kSuperK * 8;
         const int cnt = stage_kblocks(ss);
-        for (int j = 0; j < cnt; ++j) {
-          const uint32_t a_blk = smem_addr(smem + C::kOffA + s * C::kABytes + j * kTileBytes);
-          const uint32_t b_blk = smem_addr(smem + C::kOffB + s * C::kBBytes + j * C::kBBlock);
-          copy_block_scales(sfa + j * 8, a_blk + kTileDataBytes);
-          copy_block_scales(sfb + j * 8, b_blk + C::kBSfOffset);
-          const int steps = k_steps(args.k, kt_begin + (int64_t)ss * kSuperK + j);
-          for (int kk = 0; kk < steps; ++kk) {
-            const uint32_t id = (uint32_t)(kk & 1) * 2;
-            mma_mxf4(tmem, smem_desc(a_blk + kk * 32, 0, 1024, kLayoutSwizzle128),
-                     smem_desc(b_blk + kk * 32, 0, 1024, kLayoutSwizzle128), idesc_mxf4(128, C::kBRows, id, id),
-                     sfa + j * 8 + (kk >> 1) * 4, sfb + j * 8 + (kk >> 1) * 4, accumulate ? 1u : 0u);
-            accumulate = true;
+        const int64_t kt0 = kt_begin + (int64_t)ss * kSuperK;
+        // One thread issues every MMA, so per-MMA address arithmetic sits on
+        // the critical path: the descriptors are built once per stage and
+        // advanced in their start-address field (byte offset / 16; shared
+        // addresses stay below 256 KiB, so the 14-bit field cannot carry).
+        const uint64_t a_desc = smem_desc(smem_addr(smem + C::kOffA + s * C::kABytes), 0, 1024, kLayoutSwizzle128);
+        const uint64_t b_desc = smem_desc(smem_addr(smem + C::kOffB + s * C::kBBytes), 0, 1024, kLayoutSwizzle128);
+        auto issue = [&](int j, int kk) {
+          // scale-factor id (2 per 64-K step) selects the byte of the 4-byte group
+          constexpr uint32_t kIdEven = idesc_mxf4(128, C::kBRows, 0, 0), kIdOdd = idesc_mxf4(128, C::kBRows, 2, 2);
+          mma_mxf4(tmem, a_desc + (uint64_t)((j * kTileBytes + kk * 32) >> 4),
+                   b_desc + (uint64_t)((j * C::kBBlock + kk * 32) >> 4), (kk & 1) ? kIdOdd : kIdEven,
+                   sfa + j * 8 + (kk >> 1) * 4, sfb + j * 8 + (kk >> 1) * 4, accumulate ? 1u : 0u);
+          accumulate = true;
+        };
+        if (cnt == kSuperK && (kt0 + kSuperK) * kTileK <= args.k) {  // whole stage: fully unrolled
+#pragma unroll
+          for (int j = 0; j < kSuperK; ++j) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) issue(j, kk);
+          }
+        } else {  // last stage: fewer K blocks, or a K tail of 64-element steps
+          for (int j = 0; j < cnt; ++j) {
+            const int steps = k_steps(args.k, kt0 + j);
+            for (int kk = 0; kk < steps; ++kk) issue(j, kk);
           }
         }
         mma_commit(&empty[s]);
@@ -328,27 +396,33 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     __syncwarp();
   }
 
+  // Scale factors of stage ss into tensor memory (warps 2-5, one per lane
+  // quadrant): the MMA-A scales as soon as the stage's copies have landed,
+  // then (kFusedSwap: once every quantizer thread has finished the stage)
+  // the MMA-B scales; then the MMA thread may issue the stage's MMAs.
+  auto write_stage_scales = [&](int ss) -> bool {
+    const int s = ss % kStages;
+    const uint32_t ph = (uint32_t)((ss / kStages) & 1);
+    const uint32_t quad_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t sfa = quad_base + C::kAccCols + s * C::kSfColsPerStage;
+    const uint32_t sfb = sfa + kSuperK * 8;
+    const int cnt = stage_kblocks(ss);
+    if (!__all_sync(0xFFFFFFFFu, wait_bounded(&full[s], ph, abort_flag))) return false;
+    for (int j = 0; j < cnt; ++j)
+      store_block_scales(sfa + j * 8, smem + C::kOffA + s * C::kABytes + j * kTileBytes + kTileDataBytes, lane);
+    if (C::kFused && !__all_sync(0xFFFFFFFFu, wait_bounded(&act_ready[s], ph, abort_flag))) return false;
+    for (int j = 0; j < cnt; ++j)
+      store_block_scales(sfb + j * 8, smem + C::kOffB + s * C::kBBytes + j * C::kBBlock + C::kBSfOffset, lane);
+    tmem_store_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sf_ready[s]);
+    return true;
+  };
+
   if constexpr (C::kFused) {
-    // ---------------------------------------- activation quantizers (warps 2-7)
-    // The bf16 loads for all kRing K blocks of the ring are in flight at once
-    // (a register ring indexed at compile time), so DRAM latency is paid
-    // once, not once per block.  Ring position u holds K block kt0 + u, which
-    // belongs to stage slot u / kSuperK, block u % kSuperK.
-    if (warp >= 2 && warp < 2 + kQuantWarps) {
-      constexpr int kRowsPerWarp = (BN + kQuantWarps - 1) / kQuantWarps;
-      const int qw = warp - 2;
-      uint4 w[kRing][kRowsPerWarp];
-      auto load_block = [&](int64_t kt, uint4 (&dst)[kRowsPerWarp]) {
-        const int64_t col = kt * kTileK + lane * 8;
-#pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i) {
-          const int row = qw + i * kQuantWarps;
-          dst[i] = (kt < kt_end && row < args.m && col < args.k) ? ldg_nc_v4(args.act + row * args.lda + col)
-                                                                 : make_uint4(0, 0, 0, 0);
-        }
-      };
-#pragma unroll
-      for (int u = 0; u < kRing; ++u) load_block(kt_begin + u, w[u]);
+    // ------------------------------ activation quantizers (warps 2 .. 1 + BN/4)
+    if (quantizer) {
       bool aborted = false;
       for (int64_t kt0 = kt_begin; kt0 < kt_end && !aborted; kt0 += kRing) {
         const uint32_t round = (uint32_t)((kt0 - kt_begin) / kRing);
@@ -365,41 +439,47 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
             }
           }
           uint8_t* blk = smem + C::kOffB + s * C::kBBytes + j * C::kBBlock;
-#pragma unroll
-          for (int i = 0; i < kRowsPerWarp; ++i) {
-            const int row = qw + i * kQuantWarps;
-            if (row < BN) {  // uniform across the warp
-              uint32_t sbyte;
-              const uint32_t packed = quantize_lane<kUseHardwareCvt>(w[u][i], sbyte);
-              *reinterpret_cast<uint32_t*>(blk + tile_data_offset(row, lane * 4)) = packed;
-              if ((lane & 3) == 0) blk[C::kBSfOffset + tile_sf_offset(row, lane >> 2)] = (uint8_t)sbyte;
-            }
-          }
+          uint32_t sbyte;
+          const uint4 packed = quantize_block32<kUseHardwareCvt>(w[u], sbyte);
+          *reinterpret_cast<uint4*>(blk + tile_data_offset(q_row, q_blk * 16)) = packed;
+          blk[C::kBSfOffset + tile_sf_offset(q_row, q_blk)] = (uint8_t)sbyte;
+          load_block(kt + kRing, w[u]);  // refill this ring position
           if (j == kSuperK - 1 || kt == kt_end - 1) {  // stage complete
             fence_proxy_async_smem();
-            mbar_arrive(&full[s]);
+            mbar_arrive(&act_ready[s]);
+            if (warp < 6 && !write_stage_scales((int)(round * kStages + s))) aborted = true;
           }
-          load_block(kt + kRing, w[u]);  // refill this ring position
         }
       }
+    }
+  } else {
+    if (warp >= 2 && warp < 6) {
+      for (int ss = 0; ss < nss; ++ss)
+        if (!write_stage_scales(ss)) break;
     }
   }
 
   // ------------------------------------------------------------- epilogue
   //   red: [S][128/S][kRedStride] fp32 rows this rank owns, pushed by rank q
   //        into slot q (a split cluster);
-  //   stg: bf16 output tile, [BN][128] (swap-AB: rows are C rows) or
-  //        [128][BN+8], in the stage buffers, idle once the accumulator is done.
+  //   stg: bf16 output tile [128][BN+8] (kImagePlain), in the stage buffers,
+  //        idle once the accumulator is done.
   float* red = reinterpret_cast<float*>(smem + C::kOffRed);
   __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem);
   const int rows_per_rank = kTileRows / split;
   const int row_lo = rank * rows_per_rank;  // first accumulator row this CTA stores
   __syncwarp();
   if (split > 1) cluster_wait();  // every rank's barriers are initialized
-  if (warp >= 2 && warp < 6) {
+  // Warps 2-5 drain the accumulator, warp w reading tensor-memory lane
+  // quadrant w % 4; with 8 quantizer warps (kFusedSwap, BN = 32) warps 6-9
+  // take the upper half of the same quadrants' columns, so each warp stores
+  // half as many C rows.
+  if (warp >= 2 && warp < 2 + C::kEpiWarps) {
     const int quad = warp & 3;
+    const int col_lo = ((warp - 2) >> 2) * C::kEpiCols;
     const int row = quad * 32 + lane;  // accumulator row = tensor-memory lane
     const int owner = row / rows_per_rank;  // a warp's rows span two owners when each owns 16
+    const int64_t n_swap = a_tile * kTileRows + row;
     const bool ok = wait_bounded(accum, 0, abort_flag);
     tc_fence_after();
     // split: every row goes to slot `rank` of its owner's partial buffer (the
@@ -409,9 +489,9 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
                                                      C::kRedStride),
                                 (uint32_t)owner)
                   : 0u;
-    constexpr int kChunk = BN >= 32 ? 32 : 16;
+    constexpr int kChunk = C::kEpiCols >= 32 ? 32 : 16;
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += kChunk) {
+    for (int c0 = col_lo; c0 < col_lo + C::kEpiCols; c0 += kChunk) {
       uint32_t r[kChunk];
       if constexpr (kChunk == 32) {
         tmem_load_32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c0, r);
@@ -427,9 +507,19 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
                         make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
                                     __uint_as_float(r[j + 3])));
       } else if (C::kSwap) {
+        // accumulator row = C column n, accumulator column = C row: the
+        // warp's 32 lanes store 32 consecutive columns of each C row
+        if (n_swap < args.n) {
+          __nv_bfloat16* p = args.c + (int64_t)c0 * args.ldc + n_swap;
+          if (c0 + kChunk <= args.m) {
 #pragma unroll
-        for (int j = 0; j < kChunk; ++j)
-          stg[(c0 + j) * C::kStgPitch + row] = __float2bfloat16_rn(__uint_as_float(r[j]));
+            for (int j = 0; j < kChunk; ++j, p += args.ldc) *p = __float2bfloat16_rn(__uint_as_float(r[j]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j, p += args.ldc)
+              if (c0 + j < args.m) *p = __float2bfloat16_rn(__uint_as_float(r[j]));
+          }
+        }
       } else {
 #pragma unroll
         for (int j = 0; j < kChunk; j += 8) {
@@ -474,11 +564,14 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
         acc.w += v.w;
       }
       const int row = row_lo + rr;
-      if (C::kSwap) {
-        stg[(c4 * 4 + 0) * C::kStgPitch + row] = __float2bfloat16_rn(acc.x);
-        stg[(c4 * 4 + 1) * C::kStgPitch + row] = __float2bfloat16_rn(acc.y);
-        stg[(c4 * 4 + 2) * C::kStgPitch + row] = __float2bfloat16_rn(acc.z);
-        stg[(c4 * 4 + 3) * C::kStgPitch + row] = __float2bfloat16_rn(acc.w);
+      if (C::kSwap) {  // consecutive threads: consecutive C columns of C rows 4*c4 .. 4*c4+3
+        const int64_t n = a_tile * kTileRows + row;
+        const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+        if (n < args.n) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (c4 * 4 + e < args.m) args.c[(c4 * 4 + e) * args.ldc + n] = __float2bfloat16_rn(v[e]);
+        }
       } else {
         uint2 u;
         u.x = bf16x2_bits(acc.x, acc.y);
@@ -486,27 +579,12 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
         *reinterpret_cast<uint2*>(stg + row * C::kStgPitch + c4 * 4) = u;
       }
     }
-    __syncthreads();
+    if (!C::kSwap) __syncthreads();
   }
 
   // ------------------------------------------ coalesced 16-byte stores of C
-  if (C::kSwap) {
-    // stg row j = C row j; stg column r = C column a_tile*128 + r
-    const int64_t n0 = a_tile * kTileRows + row_lo;
-    const int jmax = (int)(args.m < BN ? args.m : BN);
-    const int nch = rows_per_rank / 8;
-    for (int idx = threadIdx.x; idx < jmax * nch; idx += C::kThreads) {
-      const int j = idx / nch, ch = idx % nch;
-      const int64_t n = n0 + ch * 8;
-      const __nv_bfloat16* src = stg + j * C::kStgPitch + row_lo + ch * 8;
-      __nv_bfloat16* dst = args.c + j * args.ldc + n;
-      if (n + 8 <= args.n) {
-        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-      } else {
-        for (int e = 0; e < 8 && n + e < args.n; ++e) dst[e] = src[e];
-      }
-    }
-  } else {
+  // (swap-AB stores straight from registers above)
+  if constexpr (!C::kSwap) {
     const int64_t m0 = a_tile * kTileRows;
     const int64_t n0 = b_tile * BN;
     constexpr int nch = BN / 8;
@@ -840,8 +918,12 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan) {
     p.bn = m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : 128;
     p.grid_x = ceil_div(n, kTileRows);
     const int s_max = 8;  // the kernels' kMaxSplit
+    // The cluster exchange of a split costs about 1-1.5 us (measured on
+    // GB300 for m <= 64); a 256-K block of weights streams in a fraction of
+    // that, so a split pays only while every rank keeps several K blocks:
+    // k = 512 and 2048 run unsplit, k = 7168 with n = 2112 splits 4 ways.
     int s = 1;
-    while (s < s_max && p.grid_x * s * 2 <= sms && KT / (s * 2) >= 1) s *= 2;
+    while (s < s_max && p.grid_x * s * 2 <= sms && KT / (s * 2) >= 5) s *= 2;
     if (forced) s = forced <= KT ? forced : 1;
     p.split = s;
     p.grid_y = s;

@@ -4,9 +4,10 @@
 //   quant_image_kernel  : bf16 A[m,k] -> tiled operand image (see mxfp4_device.cuh)
 //   prepack_*_kernel    : linear MXFP4 B -> tiled operand image
 //
-// One warp covers 256 consecutive K elements of one row: lane l loads 16
-// bytes (8 bf16), lanes 4j..4j+3 form 32-element block j, the block maximum
-// comes from two shuffles, and each lane writes 4 packed bytes.
+// One thread owns one 32-element scale block: it loads the block's 64 bytes,
+// forms the block maximum in registers and writes 16 packed bytes plus the
+// scale byte.  Consecutive threads take consecutive blocks of a row, so a
+// warp reads 2 KiB of contiguous bf16 and writes 512 contiguous bytes.
 #include <cuda_runtime.h>
 
 #include "mxfp4_device.cuh"
@@ -16,38 +17,33 @@
 namespace mxfp4 {
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantUnroll = 4;
+constexpr int kQuantUnroll = 4;  // blocks in flight per thread
 
 template <bool kHw>
 __global__ void __launch_bounds__(kQuantThreads)
     quant_linear_kernel(const uint16_t* __restrict__ a, int64_t m, int64_t k, int64_t lda,
                         uint8_t* __restrict__ q, uint8_t* __restrict__ scale) {
-  const int lane = threadIdx.x & 31;
-  const int64_t spans_per_row = ceil_div(k, kTileK);
-  const int64_t total = m * spans_per_row;
-  const int64_t nwarps = (int64_t)gridDim.x * (kQuantThreads / 32);
-  const int64_t warp0 = (int64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
-  const int64_t qstride = k / 2, sstride = k / 32;
-  for (int64_t base = warp0; base < total; base += nwarps * kQuantUnroll) {
-    uint4 w[kQuantUnroll];
-    int64_t row[kQuantUnroll], col[kQuantUnroll];
-    bool ok[kQuantUnroll];
+  const int64_t blocks_per_row = k / 32;
+  const int64_t total = m * blocks_per_row;
+  const int64_t nthreads = (int64_t)gridDim.x * kQuantThreads;
+  const int64_t t0 = (int64_t)blockIdx.x * kQuantThreads + threadIdx.x;
+  for (int64_t base = t0; base < total; base += nthreads * kQuantUnroll) {
+    uint4 w[kQuantUnroll][4];
+    int64_t row[kQuantUnroll], blk[kQuantUnroll];
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      const int64_t t = base + (int64_t)u * nwarps;
-      row[u] = t / spans_per_row;
-      col[u] = (t - row[u] * spans_per_row) * kTileK + lane * 8;
-      ok[u] = (t < total) && (col[u] < k);
-      w[u] = ok[u] ? ldg_nc_v4(a + row[u] * lda + col[u]) : make_uint4(0, 0, 0, 0);
+      const int64_t t = base + (int64_t)u * nthreads;
+      row[u] = t / blocks_per_row;
+      blk[u] = t - row[u] * blocks_per_row;
+      if (t < total) ldg_nc_block(a + row[u] * lda + blk[u] * 32, w[u]);
     }
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
+      if (base + (int64_t)u * nthreads >= total) continue;
       uint32_t sbyte;
-      const uint32_t packed = quantize_lane<kHw>(w[u], sbyte);
-      if (ok[u]) {
-        *reinterpret_cast<uint32_t*>(q + row[u] * qstride + col[u] / 2) = packed;
-        if ((lane & 3) == 0) scale[row[u] * sstride + col[u] / 32] = (uint8_t)sbyte;
-      }
+      const uint4 packed = quantize_block32<kHw>(w[u], sbyte);
+      *reinterpret_cast<uint4*>(q + row[u] * (k / 2) + blk[u] * 16) = packed;
+      scale[row[u] * blocks_per_row + blk[u]] = (uint8_t)sbyte;
     }
   }
 }
@@ -55,6 +51,8 @@ __global__ void __launch_bounds__(kQuantThreads)
 // Writes the A-side operand image of an m-row activation for the GEMM.
 // Rows >= m of the last row tile are left untouched (their accumulator rows
 // are never stored); K beyond k up to the tile edge is written as zeros.
+// Thread t covers block b = t % 8 of K block kt of a row, so eight
+// consecutive threads write one swizzled 128-byte row of a data tile.
 template <bool kHw>
 __global__ void __launch_bounds__(kQuantThreads)
     quant_image_kernel(const uint16_t* __restrict__ a, int64_t m, int64_t k, int64_t lda,
@@ -62,35 +60,37 @@ __global__ void __launch_bounds__(kQuantThreads)
   // Let the dependent GEMM launch now: it prefetches weights and waits for
   // this grid's completion before it reads the image.
   pdl_launch_dependents();
-  const int lane = threadIdx.x & 31;
   const int64_t kt_count = ceil_div(k, kTileK);
-  const int64_t total = m * kt_count;
-  const int64_t nwarps = (int64_t)gridDim.x * (kQuantThreads / 32);
-  const int64_t warp0 = (int64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
-  for (int64_t base = warp0; base < total; base += nwarps * kQuantUnroll) {
-    uint4 w[kQuantUnroll];
+  const int64_t total = m * kt_count * 8;
+  const int64_t nthreads = (int64_t)gridDim.x * kQuantThreads;
+  const int64_t t0 = (int64_t)blockIdx.x * kQuantThreads + threadIdx.x;
+  for (int64_t base = t0; base < total; base += nthreads * kQuantUnroll) {
+    uint4 w[kQuantUnroll][4];
     int64_t row[kQuantUnroll], kt[kQuantUnroll];
-    bool live[kQuantUnroll];
+    int b[kQuantUnroll];
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      const int64_t t = base + (int64_t)u * nwarps;
-      live[u] = t < total;
-      row[u] = t / kt_count;
-      kt[u] = t - row[u] * kt_count;
-      const int64_t col = kt[u] * kTileK + lane * 8;
-      w[u] = (live[u] && col < k) ? ldg_nc_v4(a + row[u] * lda + col) : make_uint4(0, 0, 0, 0);
-    }
-    // all-zero pieces quantize to zero nibbles and scale byte 0
+      const int64_t t = base + (int64_t)u * nthreads;
+      b[u] = (int)(t & 7);
+      row[u] = (t >> 3) / kt_count;
+      kt[u] = (t >> 3) - row[u] * kt_count;
+      const int64_t col = kt[u] * kTileK + b[u] * 32;
+      if (t < total && col < k) {
+        ldg_nc_block(a + row[u] * lda + col, w[u]);
+      } else {
 #pragma unroll
-    for (int u = 0; u < kQuantUnroll; ++u) {
-      uint32_t sbyte;
-      const uint32_t packed = quantize_lane<kHw>(w[u], sbyte);
-      if (live[u]) {
-        const int r = (int)(row[u] & (kTileRows - 1));
-        uint8_t* blk = img + image_block(row[u] / kTileRows, kt[u], kt_count);
-        *reinterpret_cast<uint32_t*>(blk + tile_data_offset(r, lane * 4)) = packed;
-        if ((lane & 3) == 0) blk[kTileDataBytes + tile_sf_offset(r, lane >> 2)] = (uint8_t)sbyte;
+        for (int i = 0; i < 4; ++i) w[u][i] = make_uint4(0, 0, 0, 0);  // K tail: zero codes, scale byte 0
       }
+    }
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      if (base + (int64_t)u * nthreads >= total) continue;
+      uint32_t sbyte;
+      const uint4 packed = quantize_block32<kHw>(w[u], sbyte);
+      const int r = (int)(row[u] & (kTileRows - 1));
+      uint8_t* tile = img + image_block(row[u] / kTileRows, kt[u], kt_count);
+      *reinterpret_cast<uint4*>(tile + tile_data_offset(r, b[u] * 16)) = packed;
+      tile[kTileDataBytes + tile_sf_offset(r, b[u])] = (uint8_t)sbyte;
     }
   }
 }
@@ -143,16 +143,14 @@ static int grid_for(int64_t work_items, int per_block) {
 
 cudaError_t launch_quant_linear(const void* a, int64_t m, int64_t k, int64_t lda, void* q, void* scale,
                                 cudaStream_t stream) {
-  const int64_t warps = m * ceil_div(k, kTileK);
-  const int grid = grid_for(warps, (kQuantThreads / 32) * kQuantUnroll);
+  const int grid = grid_for(m * (k / 32), kQuantThreads);
   quant_linear_kernel<kUseHardwareCvt><<<grid, kQuantThreads, 0, stream>>>(
       static_cast<const uint16_t*>(a), m, k, lda, static_cast<uint8_t*>(q), static_cast<uint8_t*>(scale));
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_image(const void* a, int64_t m, int64_t k, int64_t lda, void* img, cudaStream_t stream) {
-  const int64_t warps = m * ceil_div(k, kTileK);
-  const int grid = grid_for(warps, (kQuantThreads / 32) * kQuantUnroll);
+  const int grid = grid_for(m * ceil_div(k, kTileK) * 8, kQuantThreads);
   quant_image_kernel<kUseHardwareCvt><<<grid, kQuantThreads, 0, stream>>>(static_cast<const uint16_t*>(a), m, k,
                                                                           lda, static_cast<uint8_t*>(img));
   return cudaGetLastError();

@@ -85,6 +85,30 @@ def test_quant_every_block_exponent():
     _check(from_bits(arr))
 
 
+def test_quant_every_value_under_every_block_exponent():
+    """Exhaustive encoder check: for every finite bf16 anchor exponent and two
+    anchor mantissas (0x5F stays in its binade after the +0x200000 rounding,
+    0x7F rounds up into the next), every bf16 value of magnitude up to the
+    anchor's, both signs, in blocks led by the anchor (about 16.6 M values).
+    Every (element, block exponent) pair the quantizer can meet is covered,
+    including products far below the fp32 normal range."""
+    groups = []
+    for exp_field in range(0, 255):
+        for mant in (0x5F, 0x7F):
+            anchor = (exp_field << 7) | mant
+            mags = np.arange(0, anchor + 1, dtype=np.uint32)
+            vals = np.concatenate([mags, mags | 0x8000]).astype(np.uint16)
+            pad = (-vals.size) % 31
+            vals = np.concatenate([vals, np.zeros(pad, np.uint16)]).reshape(-1, 31)
+            lead = np.full((vals.shape[0], 1), anchor, np.uint16)
+            groups.append(np.concatenate([lead, vals], axis=1))
+    blocks = np.concatenate(groups)
+    pad = (-blocks.shape[0]) % 32
+    blocks = np.concatenate([blocks, np.zeros((pad, 32), np.uint16)])
+    arr = blocks.reshape(-1, 1024)
+    _check(from_bits(arr))
+
+
 def test_quant_special_blocks():
     blocks = [
         np.zeros(32, np.uint16),                                   # all +0 -> e8m0 0
