@@ -37,7 +37,7 @@
 // Warp roles: warp 0 issues bulk copies; warp 1 owns tensor memory and issues
 // the MMAs (one thread); warps 2-5 write each stage's scale factors into
 // tensor memory (tcgen05.st) and drain the accumulator; in kFusedSwap warps
-// 2 .. 1 + BN/4 quantize the activations.  Every wait is bounded: a
+// 2-9 quantize the activations.  Every wait is bounded: a
 // wait that runs out sets a device flag and the CTA winds down.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -57,8 +57,6 @@ __device__ int g_timeout_flag = 0;
 constexpr long long kWaitLimitCycles = 1ll << 31;
 constexpr long long kDrainLimitCycles = 1ll << 25;  // ~20 ms when winding down after a timeout
 constexpr int kSuperK = 2;                          // K blocks per pipeline stage
-constexpr int kStages = 2;                          // stages in the ring
-constexpr int kRing = kSuperK * kStages;            // K blocks in flight
 
 enum GemmMode : int { kFusedSwap = 0, kImageSwap = 1, kImagePlain = 2 };
 
@@ -82,15 +80,25 @@ struct Cfg {
   static constexpr bool kSwap = kMode != kImagePlain;
   // warps: 0 issues bulk copies (in the image modes the last warp issues the
   // odd stages after the first round), 1 issues MMAs, 2-5 write the scale
-  // factors to tensor memory and drain the accumulator; in kFusedSwap warps
-  // 2 .. 2 + BN/4 - 1 quantize A, one thread per row and 32-element block of
-  // a K block (BN rows x 8 blocks), and warp 0 issues the few stages alone
-  static constexpr int kQuantWarps = kFused ? BN / 4 : 0;
-  static constexpr int kEpiWarps = kQuantWarps >= 8 ? 8 : 4;  // accumulator-draining warps (from warp 2)
+  // factors to tensor memory and drain the accumulator.  kFusedSwap: warps
+  // 2-9 quantize A, one thread per (row, 32-element block) of a K block;
+  // BN = 16 needs only half of them per K block, so the threads form
+  // kQuantGroups groups that take the stage's K blocks in turn; warp 0 issues
+  // the stages after the first round alone
+  static constexpr int kQuantWarps = kFused ? 8 : 0;
+  static constexpr int kQuantGroups = kFused ? 32 / BN : 1;
+  // K blocks in a quantizer thread's register ring: two stages' worth for
+  // BN = 32, three stages (one block each) for BN = 16, within the 168
+  // registers a thread of a 10-warp CTA can have
+  static constexpr int kRing = BN >= 32 ? 2 * kSuperK : 3;
+  static constexpr int kEpiWarps = (kFused && BN >= 32) ? 8 : 4;  // accumulator-draining warps (from warp 2)
   static constexpr int kEpiCols = BN / (kEpiWarps / 4);         // accumulator columns per draining warp
   static constexpr int kThreads = kFused ? 32 * (2 + kQuantWarps) : 32 * 7;
   static constexpr int kOddProducerWarp = kFused ? 0 : kThreads / 32 - 1;
   static constexpr int kBRows = BN;                                    // MMA N (<= 128 here)
+  // stages in the ring: kFusedSwap keeps four in flight (a thin CTA's whole
+  // K range for k <= 2048, or a split rank's share), the image modes two
+  static constexpr int kStages = kFused ? 4 : 2;
   static constexpr int kABytes = kSuperK * kTileBytes;                 // MMA-A bytes per stage
   static constexpr int kBBlock = kFused ? BN * 128 + kTileSfBytes : kTileBytes;  // per K block
   static constexpr int kBSfOffset = kFused ? BN * 128 : kTileDataBytes;          // scales inside a B block
@@ -199,11 +207,11 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
-  uint64_t* empty = full + kStages;
-  uint64_t* accum = empty + kStages;
+  uint64_t* empty = full + C::kStages;
+  uint64_t* accum = empty + C::kStages;
   uint64_t* red_full = accum + 1;  // the other ranks' partial rows owned by this rank have landed
   uint64_t* act_ready = red_full + 1;      // kFusedSwap: the stage's activations are quantized
-  uint64_t* sf_ready = act_ready + kStages;  // the stage's scale factors are in tensor memory
+  uint64_t* sf_ready = act_ready + C::kStages;  // the stage's scale factors are in tensor memory
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -218,15 +226,15 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   const int nss = (int)ceil_div(kt_end - kt_begin, kSuperK);  // pipeline stages this CTA runs
 
   // kFusedSwap: the quantizer threads start loading their bf16 blocks for
-  // the first kRing K blocks right away, before any setup: DRAM latency is
-  // the long pole.  Ring position u holds K block kt0 + u (stage slot
-  // u / kSuperK, block u % kSuperK); the register ring is indexed at compile
-  // time.  Quantizer thread qt owns row qt / 8 and 32-element block qt % 8 of
-  // every K block.
+  // the first C::kRing K blocks right away, before any setup: DRAM latency is
+  // the long pole.  Ring position u holds K block kt0 + u (block u % kSuperK
+  // of its stage); the register ring is indexed at compile time.  Quantizer
+  // thread qt owns row qt / 8 and 32-element block qt % 8 of every K block.
   const bool quantizer = C::kFused && warp >= 2 && warp < 2 + C::kQuantWarps;
   const int qt = (int)threadIdx.x - 64;
-  const int q_row = qt >> 3, q_blk = qt & 7;
-  uint4 w[kRing][4];
+  const int q_row = (qt % (BN * 8)) >> 3, q_blk = qt & 7;
+  const int q_group = qt / (BN * 8);  // K block q_group + p * kQuantGroups of every stage
+  uint4 w[C::kRing][4];
   auto load_block = [&](int64_t kt, uint4 (&dst)[4]) {
     const int64_t col = kt * kTileK + q_blk * 32;
     if (kt < kt_end && q_row < args.m && col < args.k) {
@@ -236,9 +244,16 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
       for (int i = 0; i < 4; ++i) dst[i] = make_uint4(0, 0, 0, 0);
     }
   };
+  // a thread's ring: kRingStages stages of kPerStage K blocks
+  constexpr int kPerStage = kSuperK / C::kQuantGroups;
+  constexpr int kRingStages = C::kRing / kPerStage;
+  static_assert(kSuperK % C::kQuantGroups == 0 && C::kRing % kPerStage == 0, "quantizer ring shape");
+  auto ring_kt = [&](int ss, int p) -> int64_t {  // K block of the thread's p-th block in stage ss
+    return kt_begin + (int64_t)ss * kSuperK + q_group + p * C::kQuantGroups;
+  };
   if (quantizer) {
 #pragma unroll
-    for (int u = 0; u < kRing; ++u) load_block(kt_begin + u, w[u]);
+    for (int u = 0; u < C::kRing; ++u) load_block(ring_kt(u / kPerStage, u % kPerStage), w[u]);
   }
 
   // operand written by the preceding quantization kernel
@@ -269,10 +284,10 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     // The weight stream is the long pole: initialize the barriers and start
     // the first round of stages at once.  The operand the preceding kernel
     // writes is requested only after the dependency wait.
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);                   // the bulk copies' bytes
       if (C::kFused) mbar_init(&act_ready[s], C::kQuantWarps * 32);  // every quantizer thread
-      mbar_init(&sf_ready[s], 4);               // one arrival per scale-factor warp
+      mbar_init(&sf_ready[s], C::kFused ? 8 : 4);  // one arrival per scale-factor warp
       mbar_init(&empty[s], 1);
     }
     mbar_init(accum, 1);
@@ -282,7 +297,9 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     fence_mbar_init();
     if (!args.drop_copies) {
       const uint64_t pol_weights = policy_evict_first(), pol_act = policy_evict_last();
-      const int pre = nss < kStages ? nss : kStages;
+      // kFusedSwap: stage 0 here, stages 1.. from other warps after the setup
+      // barrier (the bulk copies one thread issues are serialized)
+      const int pre = C::kFused ? (nss < 1 ? nss : 1) : (nss < C::kStages ? nss : C::kStages);
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&full[i], stage_bytes(i));
         if (!kADependent) issue_a(i, i, kMode == kImagePlain ? pol_act : pol_weights);
@@ -298,14 +315,6 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     }
   }
   if (warp == 1) {
-    if (lane < 2) {  // first and last C row of this CTA's output tile
-      const int64_t r0 = C::kSwap ? 0 : a_tile * kTileRows;
-      const int64_t rows = C::kSwap ? args.m : args.m - r0;
-      const int64_t r = r0 + (lane == 0 ? 0 : (rows < kTileRows ? rows : kTileRows) - 1);
-      const int64_t col = C::kSwap ? a_tile * kTileRows : b_tile * BN;
-      if (r < args.m && col < args.n) prefetch_l1(args.c + r * args.ldc + col);
-    }
-    __syncwarp();
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
@@ -313,6 +322,11 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (C::kFused && lane == 0 && warp >= 2 && warp - 1 < C::kStages && warp - 1 < nss && !args.drop_copies) {
+    const int i = warp - 1;  // stage i of the first round, one issuing warp each
+    mbar_arrive_expect_tx(&full[i], stage_bytes(i));
+    issue_a(i, i, policy_evict_first());
+  }
   // the owners' reduction barriers must be initialized before any rank arrives on them
   if (split > 1) cluster_arrive_relaxed();
 
@@ -322,15 +336,15 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     // two slots' copies are issued by two warps and move concurrently.
     if (lane == 0) {
       const int slot = warp == 0 ? 0 : 1;
-      const int stride = C::kOddProducerWarp == 0 ? 1 : kStages;  // one producer covers every stage
+      const int stride = C::kOddProducerWarp == 0 ? 1 : C::kStages;  // one producer covers every stage
       const uint64_t pol_weights = policy_evict_first(), pol_act = policy_evict_last();
       const uint64_t pol_a = kMode == kImagePlain ? pol_act : pol_weights;
       const uint64_t pol_b = kMode == kImageSwap ? pol_act : pol_weights;
       bool waited_dependency = false;
       for (int ss = slot; ss < nss && !args.drop_copies; ss += stride) {
-        if (ss < kStages) continue;  // issued in the prologue
-        const int s = ss % kStages;
-        if (!wait_bounded(&empty[s], (uint32_t)(((ss / kStages) & 1) ^ 1), abort_flag)) break;
+        if (ss < C::kStages) continue;  // issued in the prologue
+        const int s = ss % C::kStages;
+        if (!wait_bounded(&empty[s], (uint32_t)(((ss / C::kStages) & 1) ^ 1), abort_flag)) break;
         mbar_arrive_expect_tx(&full[s], stage_bytes(ss));
         if (!kADependent) issue_a(ss, s, pol_a);
         if (!C::kFused && !kBDependent) issue_b(ss, s, pol_b);
@@ -344,9 +358,9 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
         }
       }
       if (*abort_flag) {  // let the copies in flight land before the CTA exits
-        for (int t = slot; t < kStages && t < nss; t += stride) {
-          const int last = t + ((nss - 1 - t) / kStages) * kStages;
-          wait_bounded(&full[t], (uint32_t)((last / kStages) & 1), abort_flag, kDrainLimitCycles);
+        for (int t = slot; t < C::kStages && t < nss; t += stride) {
+          const int last = t + ((nss - 1 - t) / C::kStages) * C::kStages;
+          wait_bounded(&full[t], (uint32_t)((last / C::kStages) & 1), abort_flag, kDrainLimitCycles);
         }
       }
     }
@@ -355,8 +369,8 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     if (lane == 0) {
       bool accumulate = false;
       for (int ss = 0; ss < nss; ++ss) {
-        const int s = ss % kStages;
-        const uint32_t ph = (uint32_t)((ss / kStages) & 1);
+        const int s = ss % C::kStages;
+        const uint32_t ph = (uint32_t)((ss / C::kStages) & 1);
         if (!wait_bounded(&full[s], ph, abort_flag) || !wait_bounded(&sf_ready[s], ph, abort_flag)) break;
         tc_fence_after();
         const uint32_t sfa = tmem + C::kAccCols + s * C::kSfColsPerStage;
@@ -396,23 +410,29 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     __syncwarp();
   }
 
-  // Scale factors of stage ss into tensor memory (warps 2-5, one per lane
-  // quadrant): the MMA-A scales as soon as the stage's copies have landed,
-  // then (kFusedSwap: once every quantizer thread has finished the stage)
-  // the MMA-B scales; then the MMA thread may issue the stage's MMAs.
-  auto write_stage_scales = [&](int ss) -> bool {
-    const int s = ss % kStages;
-    const uint32_t ph = (uint32_t)((ss / kStages) & 1);
+  // Scale factors of stage ss into tensor memory by a warp per 32-lane
+  // quadrant (the warp's own, warp % 4): the MMA-A scales once the stage's
+  // copies have landed, the MMA-B scales (kFusedSwap: once every quantizer
+  // thread has finished the stage); then the MMA thread may issue the stage's
+  // MMAs.  Image modes: warps 2-5 write both.  kFusedSwap: warps 6-9 write the
+  // MMA-A (weight) scales and warps 2-5 the MMA-B (activation) scales.
+  auto write_stage_scales = [&](int ss, bool do_a, bool do_b) -> bool {
+    const int s = ss % C::kStages;
+    const uint32_t ph = (uint32_t)((ss / C::kStages) & 1);
     const uint32_t quad_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t sfa = quad_base + C::kAccCols + s * C::kSfColsPerStage;
     const uint32_t sfb = sfa + kSuperK * 8;
     const int cnt = stage_kblocks(ss);
-    if (!__all_sync(0xFFFFFFFFu, wait_bounded(&full[s], ph, abort_flag))) return false;
-    for (int j = 0; j < cnt; ++j)
-      store_block_scales(sfa + j * 8, smem + C::kOffA + s * C::kABytes + j * kTileBytes + kTileDataBytes, lane);
-    if (C::kFused && !__all_sync(0xFFFFFFFFu, wait_bounded(&act_ready[s], ph, abort_flag))) return false;
-    for (int j = 0; j < cnt; ++j)
-      store_block_scales(sfb + j * 8, smem + C::kOffB + s * C::kBBytes + j * C::kBBlock + C::kBSfOffset, lane);
+    if (do_a) {
+      if (!__all_sync(0xFFFFFFFFu, wait_bounded(&full[s], ph, abort_flag))) return false;
+      for (int j = 0; j < cnt; ++j)
+        store_block_scales(sfa + j * 8, smem + C::kOffA + s * C::kABytes + j * kTileBytes + kTileDataBytes, lane);
+    }
+    if (do_b) {
+      if (!__all_sync(0xFFFFFFFFu, wait_bounded(C::kFused ? &act_ready[s] : &full[s], ph, abort_flag))) return false;
+      for (int j = 0; j < cnt; ++j)
+        store_block_scales(sfb + j * 8, smem + C::kOffB + s * C::kBBytes + j * C::kBBlock + C::kBSfOffset, lane);
+    }
     tmem_store_wait();
     tc_fence_before();
     __syncwarp();
@@ -421,41 +441,49 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   };
 
   if constexpr (C::kFused) {
-    // ------------------------------ activation quantizers (warps 2 .. 1 + BN/4)
+    // ------------------------------------- activation quantizers (warps 2-9)
     if (quantizer) {
       bool aborted = false;
-      for (int64_t kt0 = kt_begin; kt0 < kt_end && !aborted; kt0 += kRing) {
-        const uint32_t round = (uint32_t)((kt0 - kt_begin) / kRing);
+      for (int ss0 = 0; ss0 < nss && !aborted; ss0 += kRingStages) {
 #pragma unroll
-        for (int u = 0; u < kRing; ++u) {
-          const int64_t kt = kt0 + u;
-          if (kt >= kt_end || aborted) continue;
-          const int s = u / kSuperK, j = u % kSuperK;
-          if (j == 0) {
-            const bool slot_free = wait_bounded(&empty[s], (round & 1) ^ 1, abort_flag);
-            if (!__all_sync(0xFFFFFFFFu, slot_free)) {  // keep the warp's decision uniform
-              aborted = true;
-              continue;
+        for (int rs = 0; rs < kRingStages; ++rs) {
+          const int ss = ss0 + rs;
+          if (ss >= nss || aborted) continue;
+          const int s = ss % C::kStages;
+          const bool slot_free = wait_bounded(&empty[s], (uint32_t)(((ss / C::kStages) & 1) ^ 1), abort_flag);
+          if (!__all_sync(0xFFFFFFFFu, slot_free)) {  // keep the warp's decision uniform
+            aborted = true;
+            continue;
+          }
+          const int cnt = stage_kblocks(ss);
+#pragma unroll
+          for (int p = 0; p < kPerStage; ++p) {
+            const int u = rs * kPerStage + p, j = q_group + p * C::kQuantGroups;
+            if (j < cnt) {
+              uint8_t* blk = smem + C::kOffB + s * C::kBBytes + j * C::kBBlock;
+              uint32_t sbyte;
+              const uint4 packed = quantize_block32<kUseHardwareCvt>(w[u], sbyte);
+              *reinterpret_cast<uint4*>(blk + tile_data_offset(q_row, q_blk * 16)) = packed;
+              blk[C::kBSfOffset + tile_sf_offset(q_row, q_blk)] = (uint8_t)sbyte;
             }
+            load_block(ring_kt(ss + kRingStages, p), w[u]);  // refill this ring position
           }
-          uint8_t* blk = smem + C::kOffB + s * C::kBBytes + j * C::kBBlock;
-          uint32_t sbyte;
-          const uint4 packed = quantize_block32<kUseHardwareCvt>(w[u], sbyte);
-          *reinterpret_cast<uint4*>(blk + tile_data_offset(q_row, q_blk * 16)) = packed;
-          blk[C::kBSfOffset + tile_sf_offset(q_row, q_blk)] = (uint8_t)sbyte;
-          load_block(kt + kRing, w[u]);  // refill this ring position
-          if (j == kSuperK - 1 || kt == kt_end - 1) {  // stage complete
-            fence_proxy_async_smem();
-            mbar_arrive(&act_ready[s]);
-            if (warp < 6 && !write_stage_scales((int)(round * kStages + s))) aborted = true;
-          }
+          // every quantizer thread arrives once per stage, with or without a block in it
+          fence_proxy_async_smem();
+          mbar_arrive(&act_ready[s]);
+          // The quantizer warps also write the scales (2-5 activations, 6-9
+          // weights), one stage behind their quantization: by then the other
+          // quantizers have finished that stage and its weights have landed,
+          // so neither role waits on the other.
+          if (ss > 0 && !write_stage_scales(ss - 1, warp >= 6, warp < 6)) aborted = true;
         }
       }
+      if (!aborted && nss > 0) write_stage_scales(nss - 1, warp >= 6, warp < 6);
     }
   } else {
     if (warp >= 2 && warp < 6) {
       for (int ss = 0; ss < nss; ++ss)
-        if (!write_stage_scales(ss)) break;
+        if (!write_stage_scales(ss, true, true)) break;
     }
   }
 
