@@ -118,6 +118,9 @@ struct Cfg {
   static constexpr int kStgPitch = BN + 8;  // elements (kImagePlain)
   static constexpr int kStgBytes = kSwap ? 0 : 128 * kStgPitch * 2;
   static_assert(kStgBytes <= kOffBars, "output staging must fit in the stage buffers");
+  // split-K: the rows other ranks own are gathered after the staging tile
+  static constexpr int kOffOut = (kStgBytes + 1023) & ~1023;
+  static_assert(kOffOut + 128 * (BN + 4) * 4 <= kOffBars, "split-K gather buffer must fit in the stage buffers");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(kBBlock % 1024 == 0, "swizzled operand blocks must stay 1024-byte aligned");
   // tensor memory: accumulator columns, then per-stage scale-factor columns
@@ -291,10 +294,13 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
       mbar_init(&empty[s], 1);
     }
     mbar_init(accum, 1);
-    // one arrival per (other rank, warp holding some of this rank's rows)
-    mbar_init(red_full, (uint32_t)((split > 1 ? split - 1 : 1) * (split > 4 ? 1 : 4 / split) * (C::kEpiWarps / 4)));
+    // the other ranks' partial rows arrive as bulk copies: one arrival (this
+    // thread's, below) plus their bytes
+    mbar_init(red_full, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    if (split > 1)
+      mbar_arrive_expect_tx(red_full, (uint32_t)((split - 1) * (kTileRows / split) * C::kRedStride * 4));
     if (!args.drop_copies) {
       const uint64_t pol_weights = policy_evict_first(), pol_act = policy_evict_last();
       // kFusedSwap: stage 0 here, stages 1.. from other warps after the setup
@@ -510,13 +516,12 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     const int64_t n_swap = a_tile * kTileRows + row;
     const bool ok = wait_bounded(accum, 0, abort_flag);
     tc_fence_after();
-    // split: every row goes to slot `rank` of its owner's partial buffer (the
-    // owner's own rows through the same path, to its own shared memory)
-    const uint32_t dst =
-        split > 1 ? map_cluster(smem_addr(red + (size_t)(rank * rows_per_rank + (row - owner * rows_per_rank)) *
-                                                     C::kRedStride),
-                                (uint32_t)owner)
-                  : 0u;
+    // split: this rank's own rows go to its slot of `red`; the rows another
+    // rank owns are gathered per owner in the (idle) stage buffers and sent
+    // below as one bulk copy per owner
+    float* part = (owner == rank ? red + (size_t)rank * rows_per_rank * C::kRedStride
+                                 : reinterpret_cast<float*>(smem + C::kOffOut) + (size_t)owner * rows_per_rank * C::kRedStride) +
+                  (size_t)(row - owner * rows_per_rank) * C::kRedStride;
     constexpr int kChunk = C::kEpiCols >= 32 ? 32 : 16;
 #pragma unroll 1
     for (int c0 = col_lo; c0 < col_lo + C::kEpiCols; c0 += kChunk) {
@@ -531,9 +536,8 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
       if (split > 1) {
 #pragma unroll
         for (int j = 0; j < kChunk; j += 4)
-          st_cluster_f4(dst + (uint32_t)(c0 + j) * 4u,
-                        make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
-                                    __uint_as_float(r[j + 3])));
+          *reinterpret_cast<float4*>(part + c0 + j) = make_float4(
+              __uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
       } else if (C::kSwap) {
         // accumulator row = C column n, accumulator column = C row: the
         // warp's 32 lanes store 32 consecutive columns of each C row
@@ -560,14 +564,7 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
         }
       }
     }
-    if (split > 1) {
-      // The warp's pushes happen before the cluster-scope release of lane 0
-      // (and of lane 16, when the warp's rows span two owners): one arrival
-      // per warp and remote owner.
-      __syncwarp();
-      const bool first_of_owner = lane == 0 || (rows_per_rank < 32 && lane == 16);
-      if (first_of_owner && owner != rank) mbar_arrive_remote(map_cluster(smem_addr(red_full), (uint32_t)owner));
-    }
+    if (split > 1) fence_proxy_async_smem();  // the gathered rows are read by bulk copies
   }
   tc_fence_before();
   __syncthreads();
@@ -577,6 +574,17 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   }
 
   if (split > 1) {
+    // --------------- reduce-scatter: slot `rank` of every other owner's `red`
+    const uint32_t slot_bytes = (uint32_t)(rows_per_rank * C::kRedStride * 4);
+    if (threadIdx.x == 0 && !*abort_flag) {
+      for (int o = 0; o < split; ++o) {
+        if (o == rank) continue;
+        bulk_copy_to_cluster(map_cluster(smem_addr(red + (size_t)rank * rows_per_rank * C::kRedStride), (uint32_t)o),
+                             reinterpret_cast<const float*>(smem + C::kOffOut) + (size_t)o * rows_per_rank * C::kRedStride,
+                             slot_bytes, map_cluster(smem_addr(red_full), (uint32_t)o));
+      }
+      bulk_commit_group();
+    }
     // ------------------------- sum this rank's rows over the S partials, in rank order
     wait_bounded_cluster(red_full, 0, abort_flag);  // the other ranks' rows have landed
     constexpr int kC4 = BN / 4;
@@ -609,6 +617,9 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     }
     if (!C::kSwap) __syncthreads();
   }
+
+  // this CTA's outgoing bulk copies must have read their source before it exits
+  if (split > 1 && threadIdx.x == 0) bulk_wait_group_read0();
 
   // ------------------------------------------ coalesced 16-byte stores of C
   // (swap-AB stores straight from registers above)

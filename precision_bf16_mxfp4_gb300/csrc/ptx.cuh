@@ -189,11 +189,6 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Arrive on an mbarrier in another CTA of the cluster, releasing this
-// thread's prior writes (including st.shared::cluster) at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
 // try_wait that acquires writes released at cluster scope by other CTAs.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -211,10 +206,20 @@ __device__ __forceinline__ uint32_t map_cluster(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_f4(uint32_t caddr, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(caddr), "f"(v.x), "f"(v.y), "f"(v.z),
-               "f"(v.w)
-               : "memory");
+// Bulk copy from this CTA's shared memory into another CTA's shared memory
+// in the cluster; the bytes complete on an mbarrier in the destination CTA.
+// 16-byte aligned addresses, size a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_caddr, const void* src_smem, uint32_t bytes,
+                                                     uint32_t mbar_caddr) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst_caddr),
+      "r"(smem_addr(src_smem)), "r"(bytes), "r"(mbar_caddr)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the source buffers of this thread's committed bulk copies have been read.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // ------------------------------------------------ programmatic dependent launch
