@@ -78,8 +78,8 @@ template <int BN, int kMode>
 struct Cfg {
   static constexpr bool kFused = kMode == kFusedSwap;
   static constexpr bool kSwap = kMode != kImagePlain;
-  // warps: 0 issues bulk copies (in the image modes the last warp issues the
-  // odd stages after the first round), 1 issues MMAs, 2-5 write the scale
+  // warps: 0 issues the weights' bulk copies (in the image modes the last
+  // warp issues the activation image's), 1 issues MMAs, 2-5 write the scale
   // factors to tensor memory and drain the accumulator.  kFusedSwap: warps
   // 2-9 quantize A, one thread per (row, 32-element block) of a K block;
   // BN = 16 needs only half of them per K block, so the threads form
@@ -97,8 +97,8 @@ struct Cfg {
   static constexpr int kOddProducerWarp = kFused ? 0 : kThreads / 32 - 1;
   static constexpr int kBRows = BN;                                    // MMA N (<= 128 here)
   // stages in the ring: kFusedSwap keeps four in flight (a thin CTA's whole
-  // K range for k <= 2048, or a split rank's share), the image modes two
-  static constexpr int kStages = kFused ? 4 : 2;
+  // K range for k <= 2048, or a split rank's share), the image modes three
+  static constexpr int kStages = kFused ? 4 : 3;
   static constexpr int kABytes = kSuperK * kTileBytes;                 // MMA-A bytes per stage
   static constexpr int kBBlock = kFused ? BN * 128 + kTileSfBytes : kTileBytes;  // per K block
   static constexpr int kBSfOffset = kFused ? BN * 128 : kTileDataBytes;          // scales inside a B block
@@ -107,20 +107,25 @@ struct Cfg {
   static constexpr int kOffB = kOffA + kStages * kABytes;
   static constexpr int kOffBars = kOffB + kStages * kBBytes;
   static constexpr int kOffMisc = kOffBars + (4 * kStages + 2) * 8;
-  // split-K partials of the rows this rank owns land in a region of their own:
-  // another rank may push while this CTA's MMAs still read the stage buffers
+  // Once this CTA's accumulator is complete its stage buffers are idle and
+  // hold the bf16 output tile (kImagePlain) and the split-K rows other ranks
+  // own, gathered per owner.  The partials of the rows this rank owns
+  // ([S][128/S][kRedStride], slot q written by rank q) get a region of their
+  // own in kFusedSwap, so a fast rank can send while this one still runs its
+  // MMAs; the image modes need that shared memory for their third stage and
+  // keep them in the stage buffers too, sending only after a cluster barrier
+  // that follows every rank's accumulator.
   static constexpr int kMaxSplit = 8;
-  static constexpr int kRedStride = BN + 4;                   // fp32 partial-row pitch (floats)
-  static constexpr int kRedBytes = 128 * kRedStride * 4;      // [S][128/S][kRedStride]
-  static constexpr int kOffRed = (kOffMisc + 16 + 15) & ~15;
-  static constexpr int kSmemBytes = kOffRed + kRedBytes + 1024;  // + alignment slack
-  // bf16 output staging reuses the stage buffers once the accumulator is complete
-  static constexpr int kStgPitch = BN + 8;  // elements (kImagePlain)
+  static constexpr int kRedStride = BN + 4;               // fp32 partial-row pitch (floats)
+  static constexpr int kRedBytes = 128 * kRedStride * 4;
+  static constexpr bool kRedInStages = !kFused;
+  static constexpr int kStgPitch = BN + 8;                // elements (kImagePlain)
   static constexpr int kStgBytes = kSwap ? 0 : 128 * kStgPitch * 2;
-  static_assert(kStgBytes <= kOffBars, "output staging must fit in the stage buffers");
-  // split-K: the rows other ranks own are gathered after the staging tile
   static constexpr int kOffOut = (kStgBytes + 1023) & ~1023;
-  static_assert(kOffOut + 128 * (BN + 4) * 4 <= kOffBars, "split-K gather buffer must fit in the stage buffers");
+  static constexpr int kOffRed = kRedInStages ? kOffOut + ((kRedBytes + 1023) & ~1023) : (kOffMisc + 16 + 15) & ~15;
+  static_assert(kOffOut + kRedBytes <= kOffBars, "the gather buffer must fit in the stage buffers");
+  static_assert(!kRedInStages || kOffRed + kRedBytes <= kOffBars, "epilogue buffers must fit in the stage buffers");
+  static constexpr int kSmemBytes = (kRedInStages ? kOffMisc + 16 : kOffRed + kRedBytes) + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(kBBlock % 1024 == 0, "swizzled operand blocks must stay 1024-byte aligned");
   // tensor memory: accumulator columns, then per-stage scale-factor columns
@@ -259,36 +264,46 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     for (int u = 0; u < C::kRing; ++u) load_block(ring_kt(u / kPerStage, u % kPerStage), w[u]);
   }
 
-  // operand written by the preceding quantization kernel
-  constexpr bool kADependent = kMode == kImagePlain;
-  constexpr bool kBDependent = kMode == kImageSwap;
   const bool b_valid = !C::kFused && b_tile < ceil_div(args.b_rows, kTileRows);
   auto stage_kblocks = [&](int ss) -> int {
     const int64_t left = kt_end - (kt_begin + (int64_t)ss * kSuperK);
     return left < kSuperK ? (int)left : kSuperK;
   };
-  auto stage_bytes = [&](int ss) -> uint32_t {
-    const uint32_t cnt = (uint32_t)stage_kblocks(ss);
-    return cnt * kTileBytes + (b_valid ? cnt * kTileBytes : 0u);
-  };
   auto issue_a = [&](int ss, int s, uint64_t policy) {
     const int64_t kt0 = kt_begin + (int64_t)ss * kSuperK;
-    bulk_load_hint(smem + C::kOffA + s * C::kABytes, args.a_img + image_block(a_tile, kt0, KT),
-                   (uint32_t)stage_kblocks(ss) * kTileBytes, &full[s], policy);
+    const uint32_t bytes = (uint32_t)stage_kblocks(ss) * kTileBytes;
+    mbar_arrive_expect_tx(&full[s], bytes);
+    bulk_load_hint(smem + C::kOffA + s * C::kABytes, args.a_img + image_block(a_tile, kt0, KT), bytes, &full[s],
+                   policy);
   };
   auto issue_b = [&](int ss, int s, uint64_t policy) {
-    if (!b_valid) return;
+    if (!b_valid) {  // a weight row tile beyond n: nothing to copy
+      mbar_arrive(&full[s]);
+      return;
+    }
     const int64_t kt0 = kt_begin + (int64_t)ss * kSuperK;
-    bulk_load_hint(smem + C::kOffB + s * C::kBBytes, args.b_img + image_block(b_tile, kt0, KT),
-                   (uint32_t)stage_kblocks(ss) * kTileBytes, &full[s], policy);
+    const uint32_t bytes = (uint32_t)stage_kblocks(ss) * kTileBytes;
+    mbar_arrive_expect_tx(&full[s], bytes);
+    bulk_load_hint(smem + C::kOffB + s * C::kBBytes, args.b_img + image_block(b_tile, kt0, KT), bytes, &full[s],
+                   policy);
+  };
+  // Two operand streams: W, the weights, and (image modes) X, the activation
+  // image the preceding quantization kernel writes.  Each has one issuing
+  // thread (the bulk copies one thread issues are serialized) and arrives on
+  // a stage's full barrier once, with its bytes.
+  constexpr bool kWIsA = kMode != kImagePlain;
+  auto issue_w = [&](int ss, int s) {
+    if (kWIsA) issue_a(ss, s, policy_evict_first());
+    else issue_b(ss, s, policy_evict_first());
+  };
+  auto issue_x = [&](int ss, int s) {
+    if (kWIsA) issue_b(ss, s, policy_evict_last());
+    else issue_a(ss, s, policy_evict_last());
   };
 
   if (threadIdx.x == 0) {
-    // The weight stream is the long pole: initialize the barriers and start
-    // the first round of stages at once.  The operand the preceding kernel
-    // writes is requested only after the dependency wait.
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full[s], 1);                   // the bulk copies' bytes
+      mbar_init(&full[s], C::kFused ? 1 : 2);  // one arrival (with its bytes) per operand stream
       if (C::kFused) mbar_init(&act_ready[s], C::kQuantWarps * 32);  // every quantizer thread
       mbar_init(&sf_ready[s], C::kFused ? 8 : 4);  // one arrival per scale-factor warp
       mbar_init(&empty[s], 1);
@@ -302,22 +317,11 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     if (split > 1)
       mbar_arrive_expect_tx(red_full, (uint32_t)((split - 1) * (kTileRows / split) * C::kRedStride * 4));
     if (!args.drop_copies) {
-      const uint64_t pol_weights = policy_evict_first(), pol_act = policy_evict_last();
-      // kFusedSwap: stage 0 here, stages 1.. from other warps after the setup
-      // barrier (the bulk copies one thread issues are serialized)
+      // The weight stream is the long pole: its first round starts now.
+      // kFusedSwap issues stage 0 here and stages 1.. from other warps after
+      // the setup barrier.
       const int pre = C::kFused ? (nss < 1 ? nss : 1) : (nss < C::kStages ? nss : C::kStages);
-      for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(&full[i], stage_bytes(i));
-        if (!kADependent) issue_a(i, i, kMode == kImagePlain ? pol_act : pol_weights);
-        if (!C::kFused && !kBDependent) issue_b(i, i, pol_weights);
-      }
-      if (kADependent || kBDependent) {
-        pdl_wait();
-        for (int i = 0; i < pre; ++i) {
-          if (kADependent) issue_a(i, i, pol_act);
-          if (kBDependent) issue_b(i, i, pol_act);
-        }
-      }
+      for (int i = 0; i < pre; ++i) issue_w(i, i);
     }
   }
   if (warp == 1) {
@@ -328,44 +332,29 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (C::kFused && lane == 0 && warp >= 2 && warp - 1 < C::kStages && warp - 1 < nss && !args.drop_copies) {
-    const int i = warp - 1;  // stage i of the first round, one issuing warp each
-    mbar_arrive_expect_tx(&full[i], stage_bytes(i));
-    issue_a(i, i, policy_evict_first());
-  }
+  if (C::kFused && lane == 0 && warp >= 2 && warp - 1 < C::kStages && warp - 1 < nss && !args.drop_copies)
+    issue_w(warp - 1, warp - 1);  // stage i = warp - 1 of the first round, one issuing warp each
   // the owners' reduction barriers must be initialized before any rank arrives on them
   if (split > 1) cluster_arrive_relaxed();
 
   if (warp == 0 || warp == C::kOddProducerWarp) {
-    // --------------------------------- bulk-copy producers: one per stage slot
-    // The TMA engine serializes the bulk copies issued by one thread, so the
-    // two slots' copies are issued by two warps and move concurrently.
-    if (lane == 0) {
-      const int slot = warp == 0 ? 0 : 1;
-      const int stride = C::kOddProducerWarp == 0 ? 1 : C::kStages;  // one producer covers every stage
-      const uint64_t pol_weights = policy_evict_first(), pol_act = policy_evict_last();
-      const uint64_t pol_a = kMode == kImagePlain ? pol_act : pol_weights;
-      const uint64_t pol_b = kMode == kImageSwap ? pol_act : pol_weights;
-      bool waited_dependency = false;
-      for (int ss = slot; ss < nss && !args.drop_copies; ss += stride) {
-        if (ss < C::kStages) continue;  // issued in the prologue
+    // ------------------------------------------------ bulk-copy producers
+    // warp 0: the weight stream's later rounds; the last warp (image modes):
+    // the activation stream, after the quantization kernel has finished
+    if (lane == 0 && !args.drop_copies) {
+      const bool x_stream = !C::kFused && warp == C::kOddProducerWarp;
+      if (x_stream) pdl_wait();
+      int issued = x_stream ? 0 : (nss < C::kStages ? nss : C::kStages);  // the weights' first round went out at setup
+      for (int ss = issued; ss < nss; ++ss) {
         const int s = ss % C::kStages;
-        if (!wait_bounded(&empty[s], (uint32_t)(((ss / C::kStages) & 1) ^ 1), abort_flag)) break;
-        mbar_arrive_expect_tx(&full[s], stage_bytes(ss));
-        if (!kADependent) issue_a(ss, s, pol_a);
-        if (!C::kFused && !kBDependent) issue_b(ss, s, pol_b);
-        if (kADependent || kBDependent) {
-          if (!waited_dependency) {
-            pdl_wait();
-            waited_dependency = true;
-          }
-          if (kADependent) issue_a(ss, s, pol_a);
-          if (kBDependent) issue_b(ss, s, pol_b);
-        }
+        if (ss >= C::kStages && !wait_bounded(&empty[s], (uint32_t)(((ss / C::kStages) & 1) ^ 1), abort_flag)) break;
+        if (x_stream) issue_x(ss, s);
+        else issue_w(ss, s);
+        issued = ss + 1;
       }
       if (*abort_flag) {  // let the copies in flight land before the CTA exits
-        for (int t = slot; t < C::kStages && t < nss; t += stride) {
-          const int last = t + ((nss - 1 - t) / C::kStages) * C::kStages;
+        for (int t = 0; t < C::kStages && t < issued; ++t) {
+          const int last = t + ((issued - 1 - t) / C::kStages) * C::kStages;
           wait_bounded(&full[t], (uint32_t)((last / C::kStages) & 1), abort_flag, kDrainLimitCycles);
         }
       }
@@ -575,6 +564,8 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
 
   if (split > 1) {
     // --------------- reduce-scatter: slot `rank` of every other owner's `red`
+    // (in the owners' stage buffers: every rank's accumulator must be complete)
+    if (C::kRedInStages) cluster_sync();
     const uint32_t slot_bytes = (uint32_t)(rows_per_rank * C::kRedStride * 4);
     if (threadIdx.x == 0 && !*abort_flag) {
       for (int o = 0; o < split; ++o) {
