@@ -18,27 +18,31 @@
 //     weight rows.  With at least one 128 x 256 tile per SM the persistent
 //     kernel below takes over.
 // In the image modes the GEMM is launched as a programmatic dependent of the
-// quantization kernel: it streams its first weight stages first and waits for
-// the activation image only before loading it.
+// quantization kernel: it streams its first weight stages at once and waits
+// for the activation image only before loading it.
 //
 // Pipeline stages hold kSuperK consecutive K blocks (256 K each) of every
 // operand row tile, so each stage is one bulk copy per row tile: the TMA
 // engine's throughput per SM grows with the size of each copy (about
 // 40 GB/s for 16 KiB copies, 120-160 GB/s for 48-64 KiB ones, measured on
-// GB300), not with the number of copies in flight.
+// GB300), not with the number of copies in flight.  The copies one thread
+// issues are serialized, so each operand stream has its own issuing thread
+// and kFusedSwap spreads its first round of weight stages over four warps.
 //
 // K may be split across the S CTAs of a thread-block cluster.  Rank r owns
-// accumulator rows [128r/S, 128(r+1)/S): every rank writes those rows of its
-// fp32 partial into slot r of the owner's shared memory (st.shared::cluster;
-// its own rows locally) and the other ranks arrive on the owner's mbarrier
-// with cluster-scope release, one arrival per warp; the owner adds the S
-// slots in rank order (deterministic) and stores its rows.
+// accumulator rows [128r/S, 128(r+1)/S): every rank gathers the rows of its
+// fp32 partial per owner in shared memory (its own rows straight into its
+// slot) and sends each owner its rows as one DSMEM bulk copy into slot r of
+// the owner's reduction buffer, completing on the owner's mbarrier; the owner
+// adds the S slots in rank order (deterministic) and stores its rows.
 //
-// Warp roles: warp 0 issues bulk copies; warp 1 owns tensor memory and issues
+// Warp roles: warp 0 issues the weights' bulk copies (the last warp, in the
+// image modes, the activation image's); warp 1 owns tensor memory and issues
 // the MMAs (one thread); warps 2-5 write each stage's scale factors into
 // tensor memory (tcgen05.st) and drain the accumulator; in kFusedSwap warps
-// 2-9 quantize the activations.  Every wait is bounded: a
-// wait that runs out sets a device flag and the CTA winds down.
+// 2-9 quantize the activations and write the scales, and warps 6-9 also drain
+// the accumulator when BN = 32.  Every wait is bounded: a wait that runs out
+// sets a device flag and the CTA winds down.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
