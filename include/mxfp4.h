@@ -127,6 +127,56 @@ MXFP4_API mxfp4_status mxfp4_gemm(const void* a_bf16, int64_t m, int64_t k, int6
                         void* c_bf16, int64_t ldc, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * mxfp4_prepack_b_bf16 -- the on-device weight path in one call: bf16 B[n,k]
+ * (row stride ldb) straight into the prepacked image, bit-identical to
+ * mxfp4_quant followed by mxfp4_prepack_b, with no intermediate buffer.  The
+ * pages hand B in bf16 beside its MXFP4 form (submission 752099,
+ * `custom_kernel` input tuple); this quantizes it with the same rule as A.
+ *   b_bf16  : bf16 [n, k], row stride ldb elements
+ *   b_packed: u8 [b_packed_bytes], opaque; valid only for this (n, k).
+ * Preconditions: n > 0, k > 0, k % 32 == 0, ldb >= k, ldb % 8 == 0,
+ * b_packed_bytes >= mxfp4_prepacked_b_bytes(n, k), b_bf16 and b_packed
+ * 16-byte aligned.  Errors: MXFP4_ERR_INVALID_ARG, MXFP4_ERR_CUDA.
+ */
+MXFP4_API mxfp4_status mxfp4_prepack_b_bf16(const void* b_bf16, int64_t n, int64_t k, int64_t ldb, void* b_packed,
+                                            size_t b_packed_bytes, void* stream);
+
+/*
+ * Reusing one quantized activation across several GEMMs (the pages' fused
+ * "quant + scale-shuffle write" of the activation, submission 705642 v3
+ * docstring, lifted into its own call): mxfp4_quant_image writes A's MXFP4
+ * quantization directly in the tensor-core operand layout (scales already in
+ * the tensor-memory atom order), and mxfp4_gemm_image multiplies such an
+ * image by any prepacked B of the same k without quantizing again.
+ *
+ * mxfp4_act_image_bytes(m, k): bytes of the activation image (the same
+ * formula as mxfp4_prepacked_b_bytes(m, k)); 0 for invalid arguments.
+ *
+ * mxfp4_quant_image:
+ *   a_bf16  : bf16 [m, k], row stride lda elements
+ *   a_image : u8 [a_image_bytes], opaque; valid only for this (m, k).  The
+ *             padding rows of its last 128-row tile are left as they were.
+ * Preconditions: m > 0, k > 0, k % 32 == 0, lda >= k, lda % 8 == 0,
+ * a_image_bytes >= mxfp4_act_image_bytes(m, k), a_bf16 and a_image 16-byte
+ * aligned.  Errors: MXFP4_ERR_INVALID_ARG, MXFP4_ERR_CUDA.
+ *
+ * mxfp4_gemm_image: C[m,n] = bf16( A_image . B^T ) exactly as mxfp4_gemm
+ * computes it from the A the image was made of (the same quantized values;
+ * the summation order may differ from mxfp4_gemm's for m <= 32, which
+ * quantizes inside its own kernel).  Needs no workspace.  The image may be
+ * written by the kernel launched just before on the same stream
+ * (mxfp4_quant_image): the GEMM waits for that kernel before reading it.
+ * Preconditions: as mxfp4_gemm, with a_image from mxfp4_quant_image(m, k)
+ * and 16-byte aligned.  Errors: MXFP4_ERR_INVALID_ARG,
+ * MXFP4_ERR_UNSUPPORTED, MXFP4_ERR_CUDA.
+ */
+MXFP4_API size_t mxfp4_act_image_bytes(int64_t m, int64_t k);
+MXFP4_API mxfp4_status mxfp4_quant_image(const void* a_bf16, int64_t m, int64_t k, int64_t lda, void* a_image,
+                                         size_t a_image_bytes, void* stream);
+MXFP4_API mxfp4_status mxfp4_gemm_image(const void* a_image, int64_t m, int64_t k, const void* b_packed, int64_t n,
+                                        void* c_bf16, int64_t ldc, void* stream);
+
+/*
  * Size of the scratch array built into the library for mxfp4_gemm_noalloc.
  */
 #define MXFP4_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)

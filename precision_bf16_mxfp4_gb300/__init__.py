@@ -17,13 +17,17 @@ from __future__ import annotations
 from . import _lib
 from ._lib import (  # noqa: F401  (raw C-ABI names)
     Mxfp4Error,
+    mxfp4_act_image_bytes,
     mxfp4_device_status,
     mxfp4_gemm,
+    mxfp4_gemm_image,
     mxfp4_gemm_noalloc,
     mxfp4_gemm_workspace_bytes,
     mxfp4_prepack_b,
+    mxfp4_prepack_b_bf16,
     mxfp4_prepacked_b_bytes,
     mxfp4_quant,
+    mxfp4_quant_image,
     mxfp4_status_string,
     mxfp4_version,
 )
@@ -98,6 +102,62 @@ def prepack_b(b_q, b_scale) -> PackedB:
                          ctypes_void(buf.data_ptr()), nbytes, _stream_handle(b_q.device))
     _check(st, "mxfp4_prepack_b")
     return PackedB(buf, n, k)
+
+
+def prepack_b_bf16(b) -> PackedB:
+    """bf16 B [n,k] CUDA tensor -> PackedB in one call (quantized on the
+    device with the same rule as A; bit-identical to prepack_b(*quant(b)))."""
+    torch = _torch()
+    _require_cuda(b, "b")
+    if b.dtype != torch.bfloat16 or b.dim() != 2 or b.stride(1) != 1:
+        raise ValueError("b must be a 2-D bf16 tensor with unit column stride")
+    n, k = b.shape
+    nbytes = mxfp4_prepacked_b_bytes(n, k)
+    if nbytes == 0:
+        raise ValueError("unsupported (n, k)")
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=b.device)
+    st = mxfp4_prepack_b_bf16(ctypes_void(b.data_ptr()), n, k, b.stride(0), ctypes_void(buf.data_ptr()), nbytes,
+                              _stream_handle(b.device))
+    _check(st, "mxfp4_prepack_b_bf16")
+    return PackedB(buf, n, k)
+
+
+class ActImage:
+    """A quantized activation in the tensor-core operand layout: an opaque
+    uint8 device buffer valid for (m, k), reusable by several GEMMs."""
+
+    def __init__(self, buf, m: int, k: int):
+        self.buf, self.m, self.k = buf, m, k
+
+
+def quant_image(a, out=None) -> ActImage:
+    """bf16 A [m,k] CUDA tensor -> ActImage (MXFP4, operand layout)."""
+    torch = _torch()
+    _require_cuda(a, "a")
+    if a.dtype != torch.bfloat16 or a.dim() != 2 or a.stride(1) != 1:
+        raise ValueError("a must be a 2-D bf16 tensor with unit column stride")
+    m, k = a.shape
+    nbytes = mxfp4_act_image_bytes(m, k)
+    if nbytes == 0:
+        raise ValueError("unsupported (m, k)")
+    buf = out if out is not None else torch.empty(nbytes, dtype=torch.uint8, device=a.device)
+    st = mxfp4_quant_image(ctypes_void(a.data_ptr()), m, k, a.stride(0), ctypes_void(buf.data_ptr()),
+                           buf.numel() * buf.element_size(), _stream_handle(a.device))
+    _check(st, "mxfp4_quant_image")
+    return ActImage(buf, m, k)
+
+
+def gemm_image(img: ActImage, packed: PackedB, out=None):
+    """C = A_image . B^T as bf16 [m, n] for a quantized activation image."""
+    torch = _torch()
+    if img.k != packed.k:
+        raise ValueError("the activation image and packed B disagree on k")
+    m, n = img.m, packed.n
+    c = out if out is not None else torch.empty((m, n), dtype=torch.bfloat16, device=img.buf.device)
+    st = mxfp4_gemm_image(ctypes_void(img.buf.data_ptr()), m, img.k, ctypes_void(packed.buf.data_ptr()), n,
+                          ctypes_void(c.data_ptr()), c.stride(0), _stream_handle(img.buf.device))
+    _check(st, "mxfp4_gemm_image")
+    return c
 
 
 def workspace_bytes(m: int, n: int, k: int) -> int:

@@ -26,6 +26,7 @@ MXFP4_ERR_TIMEOUT = 5
 EXPORTED = (
     "mxfp4_status_string", "mxfp4_version", "mxfp4_quant", "mxfp4_prepacked_b_bytes", "mxfp4_prepack_b",
     "mxfp4_gemm_workspace_bytes", "mxfp4_gemm", "mxfp4_gemm_noalloc", "mxfp4_device_status",
+    "mxfp4_prepack_b_bf16", "mxfp4_act_image_bytes", "mxfp4_quant_image", "mxfp4_gemm_image",
 )
 
 # size of the scratch array compiled into the library for mxfp4_gemm_noalloc
@@ -73,6 +74,14 @@ def load(build_if_missing: bool = True):
         lib.mxfp4_gemm_noalloc.restype = i32
         lib.mxfp4_device_status.argtypes = [p]
         lib.mxfp4_device_status.restype = i32
+        lib.mxfp4_prepack_b_bf16.argtypes = [p, i64, i64, i64, p, sz, p]
+        lib.mxfp4_prepack_b_bf16.restype = i32
+        lib.mxfp4_act_image_bytes.argtypes = [i64, i64]
+        lib.mxfp4_act_image_bytes.restype = sz
+        lib.mxfp4_quant_image.argtypes = [p, i64, i64, i64, p, sz, p]
+        lib.mxfp4_quant_image.restype = i32
+        lib.mxfp4_gemm_image.argtypes = [p, i64, i64, p, i64, p, i64, p]
+        lib.mxfp4_gemm_image.restype = i32
         _lib = lib
         return lib
 
@@ -115,3 +124,19 @@ def mxfp4_gemm_noalloc(a_bf16, m, k, lda, b_packed, n, c_bf16, ldc, stream) -> i
 
 def mxfp4_device_status(stream) -> int:
     return int(load().mxfp4_device_status(stream))
+
+
+def mxfp4_prepack_b_bf16(b_bf16, n, k, ldb, b_packed, b_packed_bytes, stream) -> int:
+    return int(load().mxfp4_prepack_b_bf16(b_bf16, n, k, ldb, b_packed, b_packed_bytes, stream))
+
+
+def mxfp4_act_image_bytes(m, k) -> int:
+    return int(load().mxfp4_act_image_bytes(m, k))
+
+
+def mxfp4_quant_image(a_bf16, m, k, lda, a_image, a_image_bytes, stream) -> int:
+    return int(load().mxfp4_quant_image(a_bf16, m, k, lda, a_image, a_image_bytes, stream))
+
+
+def mxfp4_gemm_image(a_image, m, k, b_packed, n, c_bf16, ldc, stream) -> int:
+    return int(load().mxfp4_gemm_image(a_image, m, k, b_packed, n, c_bf16, ldc, stream))

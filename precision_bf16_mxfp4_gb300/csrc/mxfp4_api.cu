@@ -80,6 +80,39 @@ mxfp4_status mxfp4_gemm(const void* a_bf16, int64_t m, int64_t k, int64_t lda, c
                                       static_cast<cudaStream_t>(stream)));
 }
 
+mxfp4_status mxfp4_prepack_b_bf16(const void* b_bf16, int64_t n, int64_t k, int64_t ldb, void* b_packed,
+                                  size_t b_packed_bytes, void* stream) {
+  if (n <= 0 || !valid_k(k) || ldb < k || (ldb % 8) != 0) return MXFP4_ERR_INVALID_ARG;
+  if (!b_bf16 || !b_packed || !aligned16(b_bf16) || !aligned16(b_packed)) return MXFP4_ERR_INVALID_ARG;
+  if (b_packed_bytes < mxfp4_prepacked_b_bytes(n, k)) return MXFP4_ERR_INVALID_ARG;
+  return from_cuda(mxfp4::launch_quant_image(b_bf16, n, k, ldb, b_packed, static_cast<cudaStream_t>(stream),
+                                             /*zero_padding_rows=*/true));
+}
+
+size_t mxfp4_act_image_bytes(int64_t m, int64_t k) {
+  if (m <= 0 || !valid_k(k)) return 0;
+  return static_cast<size_t>(mxfp4::image_bytes(m, k));
+}
+
+mxfp4_status mxfp4_quant_image(const void* a_bf16, int64_t m, int64_t k, int64_t lda, void* a_image,
+                               size_t a_image_bytes, void* stream) {
+  if (m <= 0 || !valid_k(k) || lda < k || (lda % 8) != 0) return MXFP4_ERR_INVALID_ARG;
+  if (!a_bf16 || !a_image || !aligned16(a_bf16) || !aligned16(a_image)) return MXFP4_ERR_INVALID_ARG;
+  if (a_image_bytes < mxfp4_act_image_bytes(m, k)) return MXFP4_ERR_INVALID_ARG;
+  return from_cuda(mxfp4::launch_quant_image(a_bf16, m, k, lda, a_image, static_cast<cudaStream_t>(stream)));
+}
+
+mxfp4_status mxfp4_gemm_image(const void* a_image, int64_t m, int64_t k, const void* b_packed, int64_t n,
+                              void* c_bf16, int64_t ldc, void* stream) {
+  if (m <= 0 || n <= 0 || !valid_k(k) || ldc < n || (ldc % 8) != 0) return MXFP4_ERR_INVALID_ARG;
+  if (!a_image || !b_packed || !c_bf16 || !aligned16(a_image) || !aligned16(b_packed) || !aligned16(c_bf16))
+    return MXFP4_ERR_INVALID_ARG;
+  mxfp4::GemmPlan plan;
+  if (mxfp4::make_gemm_plan(m, n, k, &plan, /*a_image=*/true) != 0) return MXFP4_ERR_UNSUPPORTED;
+  return from_cuda(mxfp4::launch_gemm(plan, nullptr, m, k, k, b_packed, n, c_bf16, ldc, nullptr,
+                                      static_cast<cudaStream_t>(stream), a_image));
+}
+
 mxfp4_status mxfp4_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MXFP4_ERR_CUDA;
   int flag = 0;

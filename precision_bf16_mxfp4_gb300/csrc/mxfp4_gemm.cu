@@ -941,15 +941,15 @@ static int split_override() {
   return (s == 1 || s == 2 || s == 4 || s == 8) ? s : 0;
 }
 
-int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan) {
+int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan, bool a_image) {
   const int sms = num_sms();
   const int forced = split_override();
   const int64_t KT = ceil_div(k, kTileK);
   GemmPlan p{};
   if (m <= 128) {
     p.swap_ab = true;
-    p.mode = m <= 32 ? kFusedSwap : kImageSwap;
-    p.bn = m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : 128;
+    p.mode = (m <= 32 && !a_image) ? kFusedSwap : kImageSwap;
+    p.bn = p.mode == kFusedSwap ? (m <= 16 ? 16 : 32) : (m <= 64 ? 64 : 128);
     p.grid_x = ceil_div(n, kTileRows);
     const int s_max = 8;  // the kernels' kMaxSplit
     // The cluster exchange of a split costs about 1-1.5 us (measured on
@@ -961,7 +961,7 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan) {
     if (forced) s = forced <= KT ? forced : 1;
     p.split = s;
     p.grid_y = s;
-    p.workspace = p.mode == kFusedSwap ? 0 : (size_t)image_bytes(m, k);
+    p.workspace = (p.mode == kFusedSwap || a_image) ? 0 : (size_t)image_bytes(m, k);
   } else {
     p.swap_ab = false;
     p.mode = kImagePlain;
@@ -975,7 +975,7 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan) {
     if (forced) s = (forced <= KT && forced <= s_max) ? forced : 1;
     p.split = s;
     p.grid_y = nt * s;
-    p.workspace = (size_t)image_bytes(m, k);
+    p.workspace = a_image ? 0 : (size_t)image_bytes(m, k);
     if (p.bn == 256) {  // at least one 128 x 256 tile per SM: persistent tile loop
       p.persistent = true;
       p.grid_x = mt * nt < sms ? mt * nt : sms;
@@ -1093,7 +1093,7 @@ static cudaError_t launch_persistent(const GemmPlan& plan, const GemmArgs& args,
 
 cudaError_t launch_gemm(const GemmPlan& plan, const void* a_bf16, int64_t m, int64_t k, int64_t lda,
                         const void* b_image, int64_t n, void* c, int64_t ldc, void* workspace,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const void* a_image) {
   GemmArgs args{};
   args.m = m;
   args.n = n;
@@ -1117,11 +1117,14 @@ cudaError_t launch_gemm(const GemmPlan& plan, const void* a_bf16, int64_t m, int
       default: return cudaErrorInvalidValue;
     }
   }
-  cudaError_t e = launch_quant_image(a_bf16, m, k, lda, workspace, stream);
-  if (e != cudaSuccess) return e;
+  if (!a_image) {
+    cudaError_t e = launch_quant_image(a_bf16, m, k, lda, workspace, stream);
+    if (e != cudaSuccess) return e;
+    a_image = workspace;
+  }
   if (plan.mode == kImageSwap) {
     args.a_img = static_cast<const uint8_t*>(b_image);
-    args.b_img = static_cast<const uint8_t*>(workspace);
+    args.b_img = static_cast<const uint8_t*>(a_image);
     args.b_rows = m;
     switch (plan.bn) {
       case 64: return launch_one<64, kImageSwap>(plan, args, stream);
@@ -1129,7 +1132,7 @@ cudaError_t launch_gemm(const GemmPlan& plan, const void* a_bf16, int64_t m, int
       default: return cudaErrorInvalidValue;
     }
   }
-  args.a_img = static_cast<const uint8_t*>(workspace);
+  args.a_img = static_cast<const uint8_t*>(a_image);
   args.b_img = static_cast<const uint8_t*>(b_image);
   args.b_rows = n;
   if (plan.persistent) return launch_persistent(plan, args, ceil_div(m, kTileRows), ceil_div(n, PCfg::BN), stream);

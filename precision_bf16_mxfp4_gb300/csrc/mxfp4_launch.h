@@ -19,7 +19,8 @@ int num_sms();  // multiprocessors of the current device (cached per device)
 
 cudaError_t launch_quant_linear(const void* a, int64_t m, int64_t k, int64_t lda, void* q, void* scale,
                                 cudaStream_t stream);
-cudaError_t launch_quant_image(const void* a, int64_t m, int64_t k, int64_t lda, void* img, cudaStream_t stream);
+cudaError_t launch_quant_image(const void* a, int64_t m, int64_t k, int64_t lda, void* img, cudaStream_t stream,
+                               bool zero_padding_rows = false);
 cudaError_t launch_prepack(const void* bq, const void* bs, int64_t n, int64_t k, void* img, cudaStream_t stream);
 
 // GEMM execution plan chosen from (m, n, k) and the device.
@@ -34,10 +35,14 @@ struct GemmPlan {
   size_t workspace;    // bytes of caller workspace the plan needs
 };
 
-int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan);  // 0 = ok, else unsupported
+// a_image: the activation arrives as an operand image already (image modes
+// only, no workspace).  Returns 0 = ok, else unsupported.
+int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan, bool a_image = false);
+// With a_image non-null the GEMM reads that activation image instead of
+// quantizing a_bf16 into the workspace.
 cudaError_t launch_gemm(const GemmPlan& plan, const void* a_bf16, int64_t m, int64_t k, int64_t lda,
                         const void* b_image, int64_t n, void* c, int64_t ldc, void* workspace,
-                        cudaStream_t stream);
+                        cudaStream_t stream, const void* a_image = nullptr);
 
 // Device-side watchdog flag: set by a kernel whose bounded wait ran out.
 cudaError_t read_and_clear_timeout_flag(int* flag);

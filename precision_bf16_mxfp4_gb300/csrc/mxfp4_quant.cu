@@ -48,20 +48,22 @@ __global__ void __launch_bounds__(kQuantThreads)
   }
 }
 
-// Writes the A-side operand image of an m-row activation for the GEMM.
-// Rows >= m of the last row tile are left untouched (their accumulator rows
-// are never stored); K beyond k up to the tile edge is written as zeros.
-// Thread t covers block b = t % 8 of K block kt of a row, so eight
-// consecutive threads write one swizzled 128-byte row of a data tile.
+// Writes the operand image of an m-row matrix: rows [0, rows_out) of the
+// image, rows >= m as zeros (rows_out = m leaves the last row tile's padding
+// rows untouched: an activation's padding rows only reach accumulator rows
+// that are never stored; a weight image needs them zero).  K beyond k up to
+// the tile edge is written as zeros.  Thread t covers block b = t % 8 of K
+// block kt of a row, so eight consecutive threads write one swizzled
+// 128-byte row of a data tile.
 template <bool kHw>
 __global__ void __launch_bounds__(kQuantThreads)
     quant_image_kernel(const uint16_t* __restrict__ a, int64_t m, int64_t k, int64_t lda,
-                       uint8_t* __restrict__ img) {
+                       uint8_t* __restrict__ img, int64_t rows_out) {
   // Let the dependent GEMM launch now: it prefetches weights and waits for
   // this grid's completion before it reads the image.
   pdl_launch_dependents();
   const int64_t kt_count = ceil_div(k, kTileK);
-  const int64_t total = m * kt_count * 8;
+  const int64_t total = rows_out * kt_count * 8;
   const int64_t nthreads = (int64_t)gridDim.x * kQuantThreads;
   const int64_t t0 = (int64_t)blockIdx.x * kQuantThreads + threadIdx.x;
   for (int64_t base = t0; base < total; base += nthreads * kQuantUnroll) {
@@ -75,11 +77,11 @@ __global__ void __launch_bounds__(kQuantThreads)
       row[u] = (t >> 3) / kt_count;
       kt[u] = (t >> 3) - row[u] * kt_count;
       const int64_t col = kt[u] * kTileK + b[u] * 32;
-      if (t < total && col < k) {
+      if (t < total && col < k && row[u] < m) {
         ldg_nc_block(a + row[u] * lda + col, w[u]);
       } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) w[u][i] = make_uint4(0, 0, 0, 0);  // K tail: zero codes, scale byte 0
+        for (int i = 0; i < 4; ++i) w[u][i] = make_uint4(0, 0, 0, 0);  // padding: zero codes, scale byte 0
       }
     }
 #pragma unroll
@@ -149,10 +151,12 @@ cudaError_t launch_quant_linear(const void* a, int64_t m, int64_t k, int64_t lda
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_image(const void* a, int64_t m, int64_t k, int64_t lda, void* img, cudaStream_t stream) {
-  const int grid = grid_for(m * ceil_div(k, kTileK) * 8, kQuantThreads);
-  quant_image_kernel<kUseHardwareCvt><<<grid, kQuantThreads, 0, stream>>>(static_cast<const uint16_t*>(a), m, k,
-                                                                          lda, static_cast<uint8_t*>(img));
+cudaError_t launch_quant_image(const void* a, int64_t m, int64_t k, int64_t lda, void* img, cudaStream_t stream,
+                               bool zero_padding_rows) {
+  const int64_t rows_out = zero_padding_rows ? ceil_div(m, kTileRows) * kTileRows : m;
+  const int grid = grid_for(rows_out * ceil_div(k, kTileK) * 8, kQuantThreads);
+  quant_image_kernel<kUseHardwareCvt><<<grid, kQuantThreads, 0, stream>>>(
+      static_cast<const uint16_t*>(a), m, k, lda, static_cast<uint8_t*>(img), rows_out);
   return cudaGetLastError();
 }
 

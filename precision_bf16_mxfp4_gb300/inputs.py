@@ -49,6 +49,16 @@ WORKLOADS = {
                                   "compute-heavy, separate quant + GEMM"),
 }
 
+# The test shapes listed beside the benchmark shapes in the kernelbot
+# amd-mxfp4-mm submission 752099 page (its per-shape configuration table):
+# parity cases only, with the benchmark shapes' plain N(0,1) / N(0,0.02) inputs.
+TEST_SHAPES = {
+    "m8_n2112_k7168": Workload("m8_n2112_k7168", 8, 2112, 7168, "normal", 0.02, "thin, long K: split-K"),
+    "m16_n3072_k1536": Workload("m16_n3072_k1536", 16, 3072, 1536, "normal", 0.02, "fused, medium K"),
+    "m64_n3072_k1536": Workload("m64_n3072_k1536", 64, 3072, 1536, "normal", 0.02, "quant image + swap-AB"),
+    "m256_n2880_k512": Workload("m256_n2880_k512", 256, 2880, 512, "normal", 0.02, "quant image + plain GEMM"),
+}
+
 # The pair of shapes the headline metric is quoted on (m=32, k=512).
 HEADLINE = ("m32_n4096_k512", "m32_n2880_k512")
 
@@ -83,7 +93,10 @@ def make_a(w: Workload, gen: torch.Generator) -> torch.Tensor:
 
 def make_inputs(name_or_workload, seed: int = 0):
     """Return (A bf16 [m,k], B bf16 [n,k]) on the CPU for one workload."""
-    w = WORKLOADS[name_or_workload] if isinstance(name_or_workload, str) else name_or_workload
+    if isinstance(name_or_workload, str):
+        w = WORKLOADS[name_or_workload] if name_or_workload in WORKLOADS else TEST_SHAPES[name_or_workload]
+    else:
+        w = name_or_workload
     gen = torch.Generator("cpu")
     gen.manual_seed(seed)
     a = make_a(w, gen)

@@ -111,6 +111,31 @@ def test_quant_and_prepack_reject_bad_arguments_without_a_gpu():
     assert mx.mxfp4_prepack_b(fake, fake, 0, 64, fake, 1 << 20, None) == E
 
 
+@pytest.mark.parametrize("m,k", [(4, 512), (33, 64), (4096, 2048), (129, 288)])
+def test_act_image_size(m, k):
+    assert mx.mxfp4_act_image_bytes(m, k) == _image_bytes(m, k)
+    assert mx.mxfp4_act_image_bytes(0, k) == 0
+    assert mx.mxfp4_act_image_bytes(m, 48) == 0
+
+
+def test_image_entry_points_reject_bad_arguments_without_a_gpu():
+    fake = P(0x10000)
+    E = _lib.MXFP4_ERR_INVALID_ARG
+    big = 1 << 30
+    assert mx.mxfp4_prepack_b_bf16(fake, 16, 64, 32, fake, big, None) == E           # ldb < k
+    assert mx.mxfp4_prepack_b_bf16(fake, 16, 64, 68, fake, big, None) == E           # ldb % 8
+    assert mx.mxfp4_prepack_b_bf16(fake, 16, 48, 48, fake, big, None) == E           # k % 32
+    assert mx.mxfp4_prepack_b_bf16(fake, 16, 64, 64, fake, 10, None) == E            # buffer too small
+    assert mx.mxfp4_prepack_b_bf16(P(0x10008), 16, 64, 64, fake, big, None) == E     # unaligned B
+    assert mx.mxfp4_quant_image(fake, 0, 64, 64, fake, big, None) == E               # m == 0
+    assert mx.mxfp4_quant_image(fake, 4, 64, 64, fake, 10, None) == E                # image too small
+    assert mx.mxfp4_quant_image(None, 4, 64, 64, fake, big, None) == E               # null A
+    assert mx.mxfp4_gemm_image(fake, 4, 64, fake, 16, fake, 12, None) == E           # ldc < n
+    assert mx.mxfp4_gemm_image(fake, 4, 48, fake, 16, fake, 16, None) == E           # k % 32
+    assert mx.mxfp4_gemm_image(None, 4, 64, fake, 16, fake, 16, None) == E           # null image
+    assert mx.mxfp4_gemm_image(fake, 4, 64, fake, 16, P(0x10008), 16, None) == E     # unaligned C
+
+
 def test_product_path_does_not_touch_the_oracle():
     pkg = os.path.join(ROOT, "precision_bf16_mxfp4_gb300")
     for dirpath, _, files in os.walk(pkg):

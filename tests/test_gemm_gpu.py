@@ -53,6 +53,14 @@ def test_gemm_workload_full_output(name):
     assert_close_to_ref(got, ref, what=name)
 
 
+@pytest.mark.parametrize("name", list(inputs.TEST_SHAPES))
+def test_gemm_page_test_shapes_full_output(name):
+    a, b = inputs.make_inputs(name)
+    packed, bq, bs = packed_from_oracle(b)
+    got, _ = _run(a, packed)
+    assert_close_to_ref(got, _oracle_full(a, bq, bs), what=name)
+
+
 def test_gemm_large_workload_sampled():
     name = "m4096_n7168_k2048"
     a, b = inputs.make_inputs(name)
@@ -178,6 +186,40 @@ def test_gemm_every_split_factor(m, n, k, split, monkeypatch):
     c2 = mx.gemm(a_dev, packed, out=torch.empty((m, ldc), dtype=torch.bfloat16, device="cuda")[:, :n])
     torch.cuda.synchronize()
     assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+
+
+@pytest.mark.parametrize("n,k", [(300, 544), (2880, 512), (129, 288), (2112, 7168)])
+def test_prepack_b_bf16_equals_quant_then_prepack(n, k):
+    """The one-call weight path writes the same image bytes as mxfp4_quant
+    followed by mxfp4_prepack_b (padding rows and the K tail zero)."""
+    b = inputs.random_bf16(n, k, seed=n + k, std=0.5).cuda()
+    one = mx.prepack_b_bf16(b)
+    two = mx.prepack_b(*mx.quant(b))
+    torch.cuda.synchronize()
+    assert torch.equal(one.buf, two.buf)
+
+
+@pytest.mark.parametrize("m,n,k", [(4, 2880, 512), (32, 520, 2080), (33, 256, 512), (64, 384, 2048),
+                                   (200, 256, 2048), (1000, 4856, 544)])
+def test_quant_image_then_gemm_image(m, n, k):
+    """A quantized once into the operand layout, multiplied by two different
+    weights: both products match the oracle, and for m > 32 (the same plan
+    as mxfp4_gemm) they equal mxfp4_gemm bit for bit."""
+    a = inputs.random_bf16(m, k, seed=m * 7 + k)
+    img = mx.quant_image(a.cuda())
+    for seed in (1, 2):
+        b = inputs.random_bf16(n, k, seed=n + seed, std=0.3)
+        packed, bq, bs = packed_from_oracle(b)
+        ldc = n + (8 - n % 8) % 8
+        c_full = torch.full((m, ldc), float("nan"), dtype=torch.bfloat16, device="cuda")
+        got = mx.gemm_image(img, packed, out=c_full[:, :n])
+        torch.cuda.synchronize()
+        assert_close_to_ref(got.float().cpu().numpy(), _oracle_full(a, bq, bs), what=f"gemm_image seed {seed}")
+        assert torch.isnan(c_full[:, n:].float()).all()
+        if m > 32:
+            ref = mx.gemm(a.cuda(), packed)
+            torch.cuda.synchronize()
+            assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
 
 
 def test_persistent_tile_loop_with_ragged_tails():
