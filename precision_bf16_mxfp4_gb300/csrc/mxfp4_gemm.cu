@@ -840,15 +840,22 @@ __global__ void __launch_bounds__(PCfg::kThreads, 1)
             const uint64_t bd0 = smem_desc(b0, 0, 1024, kLayoutSwizzle128);
             const uint64_t bd1 = smem_desc(b1, 0, 1024, kLayoutSwizzle128);
             const int steps = k_steps(args.k, (int64_t)ss * P::kSuperK + j);
-            for (int kk = 0; kk < steps; ++kk) {
-              // advancing the start address by 32 bytes = 2 in the descriptor's 16-byte units
-              const uint64_t adv = (uint64_t)(kk * 2);
-              const uint32_t id = (uint32_t)(kk & 1) * 2;
-              const uint32_t acc = accumulate ? 1u : 0u;
-              const uint32_t sfk = (uint32_t)(kk >> 1) * 4;
-              mma_mxf4(tmem, ad + adv, bd0 + adv, idesc_mxf4(128, 128, id, id), sf + sfk, sf + 8 + sfk, acc);
-              mma_mxf4(tmem + 128, ad + adv, bd1 + adv, idesc_mxf4(128, 128, id, id), sf + sfk, sf + 16 + sfk, acc);
+            if (steps == 4) {  // a whole K block: its eight MMAs in one go
+              mma_mxf4_kblock_n256(tmem, ad, bd0, bd1, idesc_mxf4(128, 128, 0, 0), idesc_mxf4(128, 128, 2, 2), sf,
+                                   sf + 8, sf + 16, accumulate ? 1u : 0u);
               accumulate = true;
+            } else {
+              for (int kk = 0; kk < steps; ++kk) {
+                // advancing the start address by 32 bytes = 2 in the descriptor's 16-byte units
+                const uint64_t adv = (uint64_t)(kk * 2);
+                const uint32_t id = (uint32_t)(kk & 1) * 2;
+                const uint32_t acc = accumulate ? 1u : 0u;
+                const uint32_t sfk = (uint32_t)(kk >> 1) * 4;
+                mma_mxf4(tmem, ad + adv, bd0 + adv, idesc_mxf4(128, 128, id, id), sf + sfk, sf + 8 + sfk, acc);
+                mma_mxf4(tmem + 128, ad + adv, bd1 + adv, idesc_mxf4(128, 128, id, id), sf + sfk, sf + 16 + sfk,
+                         acc);
+                accumulate = true;
+              }
             }
           }
           mma_commit(&empty[s]);

@@ -109,6 +109,35 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// The eight MMAs of one 256-K block for a 128 x 256 accumulator held as two
+// N = 128 halves (d, d + 128): four 64-K steps, each into both halves.  One
+// asm block with every operand ready: the MMA queue is shallow, so address
+// arithmetic between single MMAs would leave the tensor pipe idle.  The
+// descriptors advance 32 bytes (2 units) per step; scale ids alternate 0/2
+// (even/odd idesc); the scale columns advance 4 per two steps.
+__device__ __forceinline__ void mma_mxf4_kblock_n256(uint32_t d, uint64_t a, uint64_t b0, uint64_t b1,
+                                                     uint32_t idesc_even, uint32_t idesc_odd, uint32_t sfa,
+                                                     uint32_t sfb0, uint32_t sfb1, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, a2, a3, c1, c2, c3, e1, e2, e3;\n\t.reg .b32 d1, sa1, sb1, sc1;\n\t"
+      "setp.ne.b32 p, %9, 0;\n\tsetp.eq.b32 q, %9, %9;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+      "add.s64 c1, %2, 2;\n\tadd.s64 c2, %2, 4;\n\tadd.s64 c3, %2, 6;\n\t"
+      "add.s64 e1, %3, 2;\n\tadd.s64 e2, %3, 4;\n\tadd.s64 e3, %3, 6;\n\t"
+      "add.u32 d1, %0, 128;\n\tadd.u32 sa1, %6, 4;\n\tadd.u32 sb1, %7, 4;\n\tadd.u32 sc1, %8, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %4, [%6], [%7], p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [d1], %1, %3, %4, [%6], [%8], p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], a1, c1, %5, [%6], [%7], q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [d1], a1, e1, %5, [%6], [%8], q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], a2, c2, %4, [sa1], [sb1], q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [d1], a2, e2, %4, [sa1], [sc1], q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], a3, c3, %5, [sa1], [sb1], q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [d1], a3, e3, %5, [sa1], [sc1], q;\n\t}"
+      ::"r"(d), "l"(a), "l"(b0), "l"(b1), "r"(idesc_even), "r"(idesc_odd), "r"(sfa), "r"(sfb0), "r"(sfb1),
+      "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued
 // before it has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
