@@ -661,10 +661,12 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
 // 9 MMA issuer, 10-11 weight copies.
 struct PCfg {
   static constexpr int BN = 256;
-  // ring depth and K blocks per stage: four single-block stages keep as many
-  // bytes in flight as two double-block ones but recycle slots twice as often
-  static constexpr int kStages = 4;
-  static constexpr int kSuperK = 1;
+  // ring depth and K blocks per stage: two double-block stages keep as many
+  // bytes in flight as four single-block ones, with half as many barrier
+  // hand-offs and MMA commits (each commit costs the tensor pipe ~140 cycles,
+  // measured on GB300)
+  static constexpr int kStages = 2;
+  static constexpr int kSuperK = 2;
   static constexpr int kThreads = 32 * 12;
   static constexpr int kBTiles = 2;
   static constexpr int kABytes = kSuperK * kTileBytes;
@@ -672,7 +674,9 @@ struct PCfg {
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kStages * kABytes;
   static constexpr int kOffStg = kOffB + kStages * kBBytes;
-  static constexpr int kStgPitch = 24;  // bf16 elements per staged row (16 + 8 pad)
+  // epilogue staging: per warp, 32 rows x 32 columns of bf16 (+8 pad)
+  static constexpr int kStgCols = 32;
+  static constexpr int kStgPitch = kStgCols + 8;
   static constexpr int kStgWarpBytes = 32 * kStgPitch * 2;
   static constexpr int kOffBars = kOffStg + 4 * kStgWarpBytes;
   static constexpr int kNumBars = 3 * kStages + 2;  // full, sf_full, empty per stage; acc_full, acc_empty
@@ -892,17 +896,25 @@ __global__ void __launch_bounds__(PCfg::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);  // accumulator free for the next tile
       if (!ok) continue;
+      // 32-column chunks through the warp's staging slice: each lane writes
+      // its row's 64 bytes, then every store instruction covers eight 64-byte
+      // row segments (few, wide transactions for the LSU, which the
+      // scale-factor warps' shared loads share)
 #pragma unroll
-      for (int c = 0; c < P::BN / 16; ++c) {
+      for (int cc = 0; cc < P::BN / P::kStgCols; ++cc) {
         uint4* row_dst = reinterpret_cast<uint4*>(stg + lane * P::kStgPitch);
-        row_dst[0] = make_uint4(packed[c][0], packed[c][1], packed[c][2], packed[c][3]);
-        row_dst[1] = make_uint4(packed[c][4], packed[c][5], packed[c][6], packed[c][7]);
+#pragma unroll
+        for (int q = 0; q < P::kStgCols / 8; ++q) {
+          const int c = cc * (P::kStgCols / 16) + (q >> 1), h = q & 1;
+          row_dst[q] = make_uint4(packed[c][4 * h], packed[c][4 * h + 1], packed[c][4 * h + 2], packed[c][4 * h + 3]);
+        }
         __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int row = i * 16 + (lane >> 1), ch = lane & 1;
+        for (int i = 0; i < 32 * P::kStgCols / 256; ++i) {  // 256 columns x rows per instruction
+          constexpr int kLanesPerRow = P::kStgCols / 8;
+          const int row = i * (32 / kLanesPerRow) + lane / kLanesPerRow, ch = lane % kLanesPerRow;
           const int64_t mi = m0 + row;
-          const int64_t n = n0 + c * 16 + ch * 8;
+          const int64_t n = n0 + cc * P::kStgCols + ch * 8;
           if (mi < args.m && n < args.n) {
             const __nv_bfloat16* src = stg + row * P::kStgPitch + ch * 8;
             __nv_bfloat16* dst = args.c + mi * args.ldc + n;
