@@ -390,16 +390,26 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
                    sfa + j * 8 + (kk >> 1) * 4, sfb + j * 8 + (kk >> 1) * 4, accumulate ? 1u : 0u);
           accumulate = true;
         };
-        if (cnt == kSuperK && (kt0 + kSuperK) * kTileK <= args.k) {  // whole stage: fully unrolled
+        // a whole K block's four MMAs go out from one asm block; a K tail of
+        // 64-element steps one MMA at a time
+        auto kblock = [&](int j) {
+          constexpr uint32_t kIdEven = idesc_mxf4(128, C::kBRows, 0, 0), kIdOdd = idesc_mxf4(128, C::kBRows, 2, 2);
+          mma_mxf4_kblock(tmem, a_desc + (uint64_t)((j * kTileBytes) >> 4),
+                          b_desc + (uint64_t)((j * C::kBBlock) >> 4), kIdEven, kIdOdd, sfa + j * 8, sfb + j * 8,
+                          accumulate ? 1u : 0u);
+          accumulate = true;
+        };
+        if (cnt == kSuperK && (kt0 + kSuperK) * kTileK <= args.k) {  // whole stage
 #pragma unroll
-          for (int j = 0; j < kSuperK; ++j) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) issue(j, kk);
-          }
-        } else {  // last stage: fewer K blocks, or a K tail of 64-element steps
+          for (int j = 0; j < kSuperK; ++j) kblock(j);
+        } else {  // last stage: fewer K blocks, or a K tail
           for (int j = 0; j < cnt; ++j) {
             const int steps = k_steps(args.k, kt0 + j);
-            for (int kk = 0; kk < steps; ++kk) issue(j, kk);
+            if (steps == 4) {
+              kblock(j);
+            } else {
+              for (int kk = 0; kk < steps; ++kk) issue(j, kk);
+            }
           }
         }
         mma_commit(&empty[s]);

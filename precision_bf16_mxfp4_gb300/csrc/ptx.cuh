@@ -109,6 +109,24 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// The four MMAs of one 256-K block (four 64-K steps) into one accumulator,
+// from one asm block with every operand ready (see below).
+__device__ __forceinline__ void mma_mxf4_kblock(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc_even,
+                                                uint32_t idesc_odd, uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, a2, a3, c1, c2, c3;\n\t.reg .b32 sa1, sb1;\n\t"
+      "setp.ne.b32 p, %7, 0;\n\tsetp.eq.b32 q, %7, %7;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+      "add.s64 c1, %2, 2;\n\tadd.s64 c2, %2, 4;\n\tadd.s64 c3, %2, 6;\n\t"
+      "add.u32 sa1, %5, 4;\n\tadd.u32 sb1, %6, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], a1, c1, %4, [%5], [%6], q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], a2, c2, %3, [sa1], [sb1], q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], a3, c3, %4, [sa1], [sb1], q;\n\t}"
+      ::"r"(d), "l"(a), "l"(b), "r"(idesc_even), "r"(idesc_odd), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
 // The eight MMAs of one 256-K block for a 128 x 256 accumulator held as two
 // N = 128 halves (d, d + 128): four 64-K steps, each into both halves.  One
 // asm block with every operand ready: the MMA queue is shallow, so address
