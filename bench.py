@@ -282,9 +282,9 @@ def print_table(dev, flush, mx, inputs, hbm_gbs, table_iters=200):
 
 
 # ------------------------------------------------------------ CPU oracle
-def oracle_step_sample(names, fraction):
-    """The oracle (quant of A, then the fp64 GEMM) on the first `fraction` of
-    each shape's output columns.  Returns (seconds, algorithmic bytes covered)."""
+def _oracle_prepare(names, fraction):
+    """Inputs for the oracle step: each shape's A and the first `fraction` of
+    its weight rows (output columns), B quantized by the oracle."""
     import oracle
     from precision_bf16_mxfp4_gb300 import inputs
     prepared = []
@@ -295,6 +295,13 @@ def oracle_step_sample(names, fraction):
         bits = lambda t: t.contiguous().view(__import__("torch").int16).numpy().view("uint16")
         bq, bs = oracle.quant(bits(b[:ns]))
         prepared.append((w, bits(a), bq, bs, ns))
+    return prepared
+
+
+def _oracle_run(prepared):
+    """The oracle (quant of A, then the fp64 GEMM) on prepared inputs.
+    Returns (seconds, algorithmic bytes covered)."""
+    import oracle
     t0 = time.perf_counter()
     covered = 0
     for w, a_bits, bq, bs, ns in prepared:
@@ -304,14 +311,21 @@ def oracle_step_sample(names, fraction):
     return time.perf_counter() - t0, covered
 
 
+def oracle_step_sample(names, fraction):
+    """The oracle on the first `fraction` of each shape's output columns."""
+    return _oracle_run(_oracle_prepare(names, fraction))
+
+
 def cpu_baseline(names, budget_s=12.0):
-    t, covered = oracle_step_sample(names, 0.125)
-    reps = max(1, min(8, int(budget_s / max(t, 1e-3))))
-    total_t, total_b = t, covered
-    for _ in range(reps - 1):
-        dt, cb = oracle_step_sample(names, 0.125)
+    """The oracle on 1/8 of each shape's output columns, repeated until about
+    `budget_s` seconds of single-threaded CPU work have been timed."""
+    prepared = _oracle_prepare(names, 0.125)
+    total_t, total_b, reps = 0.0, 0, 0
+    while total_t < budget_s and reps < 10000:
+        dt, cb = _oracle_run(prepared)
         total_t += dt
         total_b += cb
+        reps += 1
     return {"value": round(total_b / total_t / 1e12, 9), "unit": "TB/s", "cores": 1, "kind": "oracle",
             "sample": f"{reps} x (quant of A + fp64 GEMM on 1/8 of each shape's output columns), "
                       f"single-threaded C, {total_t:.1f} s"}
