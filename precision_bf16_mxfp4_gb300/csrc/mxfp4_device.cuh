@@ -25,8 +25,9 @@ namespace mxfp4 {
 //     chunk c ^ (r & 7));
 //   bytes [16384, 17408): the e8m0 scales as two 512-byte atoms (K blocks
 //     0-3, 4-7); inside an atom, row r and block b sit at
-//     (r % 32) * 16 + (r / 32) * 4 + b, the 32-lane x 16-byte shape that
-//     tcgen05.cp copies into tensor memory.
+//     (r % 32) * 16 + (r / 32) * 4 + b, the 32-lane x 16-byte shape of a
+//     tensor-memory lane quadrant's scale columns (the kernels store each
+//     atom row into its lane with tcgen05.st).
 // Rows beyond R and K beyond the matrix are zero in the weight image.
 constexpr int kTileRows = 128;
 constexpr int kTileK = 256;

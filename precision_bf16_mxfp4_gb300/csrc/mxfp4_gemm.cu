@@ -187,12 +187,6 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Scale factors of one K block (two 512-byte atoms) into 8 tensor-memory columns.
-__device__ __forceinline__ void copy_block_scales(uint32_t tmem_col, uint32_t sf_smem) {
-  tmem_copy_32x128b_x4(tmem_col, smem_desc(sf_smem, 0, 128, kLayoutNoSwizzle));
-  tmem_copy_32x128b_x4(tmem_col + 4, smem_desc(sf_smem + kAtomBytes, 0, 128, kLayoutNoSwizzle));
-}
-
 // Scale factors of one K block (two 512-byte atoms in shared memory) into 8
 // tensor-memory columns of the calling warp's 32-lane quadrant, with the
 // column contents tcgen05.cp.32x128b.warpx4 would produce: lane l holds the

@@ -163,12 +163,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// Copy a 32-row x 16-byte block of shared memory into tensor memory,
-// replicated into all four 32-lane quadrants.
-__device__ __forceinline__ void tmem_copy_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // Each thread of the warp reads 16 consecutive 32-bit columns of its lane.
 __device__ __forceinline__ void tmem_load_16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
