@@ -86,7 +86,7 @@ MXFP4_API size_t mxfp4_prepacked_b_bytes(int64_t n, int64_t k);
  * mxfp4_prepack_b -- one-time repack of MXFP4 B into the layout the tensor
  * cores read: tiles of 128 rows x 256 K elements, data in the 128-byte
  * swizzled K-major order and e8m0 scales in the 32-lane x 16-byte atoms
- * that tcgen05.cp moves into tensor memory.  This replaces the pages'
+ * of a tensor-memory lane quadrant's scale columns.  This replaces the pages'
  * AMD-specific B_shuffle / `e8m0_shuffle` scale layout (submission 739530,
  * `_sh_row` / `_sh_col`), which exists only for the MI355X MFMA lane order.
  *   b_fp4   : u8 [n, k/2] as produced by mxfp4_quant (dense rows)
