@@ -280,7 +280,20 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
       return;
     }
     const int64_t kt0 = kt_begin + (int64_t)ss * kSuperK;
-    const uint32_t bytes = (uint32_t)stage_kblocks(ss) * kTileBytes;
+    const int cnt = stage_kblocks(ss);
+    if (kMode == kImageSwap && BN < kTileRows) {
+      // the MMA reads only the first BN rows of each activation block: copy
+      // those rows' data and the block's scale atoms, not the whole block
+      mbar_arrive_expect_tx(&full[s], (uint32_t)cnt * (BN * 128 + kTileSfBytes));
+      for (int j = 0; j < cnt; ++j) {
+        const uint8_t* src = args.b_img + image_block(b_tile, kt0 + j, KT);
+        uint8_t* dst = smem + C::kOffB + s * C::kBBytes + j * C::kBBlock;
+        bulk_load_hint(dst, src, BN * 128, &full[s], policy);
+        bulk_load_hint(dst + kTileDataBytes, src + kTileDataBytes, kTileSfBytes, &full[s], policy);
+      }
+      return;
+    }
+    const uint32_t bytes = (uint32_t)cnt * kTileBytes;
     mbar_arrive_expect_tx(&full[s], bytes);
     bulk_load_hint(smem + C::kOffB + s * C::kBBytes, args.b_img + image_block(b_tile, kt0, KT), bytes, &full[s],
                    policy);
