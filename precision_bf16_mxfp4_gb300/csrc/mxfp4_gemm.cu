@@ -98,7 +98,7 @@ struct Cfg {
   static constexpr int kEpiWarps = (kFused && BN >= 32) ? 8 : 4;  // accumulator-draining warps (from warp 2)
   static constexpr int kEpiCols = BN / (kEpiWarps / 4);         // accumulator columns per draining warp
   static constexpr int kThreads = kFused ? 32 * (2 + kQuantWarps) : 32 * 7;
-  static constexpr int kOddProducerWarp = kFused ? 0 : kThreads / 32 - 1;
+  static constexpr int kActProducerWarp = kFused ? 0 : kThreads / 32 - 1;  // issues the activation stream
   static constexpr int kBRows = BN;                                    // MMA N (<= 128 here)
   // stages in the ring: kFusedSwap keeps four in flight (a thin CTA's whole
   // K range for k <= 2048, or a split rank's share), the image modes three
@@ -193,7 +193,7 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
 // 16 bytes of atom row l (row groups l, l+32, l+64, l+96; K blocks 0-3) in 4
 // columns and the second atom's 16 bytes (K blocks 4-7) in the next 4.
 // Measured on GB300, a tcgen05.cp stalls the MMA queue for hundreds of
-// cycles; these stores run on the warps that have nothing else to do.
+// cycles; these stores run on warps other than the MMA issuer.
 __device__ __forceinline__ void store_block_scales(uint32_t taddr, const uint8_t* sf_smem, int lane) {
   const uint4 lo = *reinterpret_cast<const uint4*>(sf_smem + lane * 16);
   const uint4 hi = *reinterpret_cast<const uint4*>(sf_smem + kAtomBytes + lane * 16);
@@ -348,12 +348,12 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   // the owners' reduction barriers must be initialized before any rank arrives on them
   if (split > 1) cluster_arrive_relaxed();
 
-  if (warp == 0 || warp == C::kOddProducerWarp) {
+  if (warp == 0 || warp == C::kActProducerWarp) {
     // ------------------------------------------------ bulk-copy producers
     // warp 0: the weight stream's later rounds; the last warp (image modes):
     // the activation stream, after the quantization kernel has finished
     if (lane == 0 && !args.drop_copies) {
-      const bool x_stream = !C::kFused && warp == C::kOddProducerWarp;
+      const bool x_stream = !C::kFused && warp == C::kActProducerWarp;
       if (x_stream) pdl_wait();
       int issued = x_stream ? 0 : (nss < C::kStages ? nss : C::kStages);  // the weights' first round went out at setup
       for (int ss = issued; ss < nss; ++ss) {
