@@ -15,8 +15,8 @@
 //   kImageSwap (32 < m <= 128): swap-AB; MMA-B = the first BN rows of the
 //     activation image that quant_image_kernel wrote into the workspace.
 //   kImagePlain (m > 128, few tiles): MMA-A = activation image, MMA-B = 128
-//     weight rows.  With at least one 128 x 256 tile per SM the persistent
-//     kernel below takes over.
+//     weight rows.  With at least one 128 x 256 tile per SM the CTA-pair
+//     kernel below takes over (256 x 256 tiles, tcgen05 cta_group::2).
 // In the image modes the GEMM is launched as a programmatic dependent of the
 // quantization kernel: it streams its first weight stages at once and waits
 // for the activation image only before loading it.
@@ -166,12 +166,38 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
   }
 }
 
+// Winding down after a timeout: wait up to kDrainLimitCycles for a phase
+// (the bulk copies this CTA issued must land before it exits), whatever the
+// abort flag says.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < kDrainLimitCycles) {
+  }
+}
+
 // Same, acquiring at cluster scope (for phases completed by other CTAs' arrivals).
 __device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        raise_timeout(abort_flag);
+        return false;
+      }
+    }
+  }
+}
+
+// Same, polling with test_wait (for waits on arrivals from the other CTA of
+// a pair, which a suspended try_wait notices late).
+__device__ __forceinline__ bool wait_bounded_poll(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_test_wait_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_wait_cluster(bar, parity)) return true;
     if ((it & 63) == 0) {
       if (*abort_flag) return false;
       if (clock64() - t0 > kWaitLimitCycles) {
@@ -366,7 +392,7 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
       if (*abort_flag) {  // let the copies in flight land before the CTA exits
         for (int t = 0; t < C::kStages && t < issued; ++t) {
           const int last = t + ((issued - 1 - t) / C::kStages) * C::kStages;
-          wait_bounded(&full[t], (uint32_t)((last / C::kStages) & 1), abort_flag, kDrainLimitCycles);
+          drain_wait(&full[t], (uint32_t)((last / C::kStages) & 1));
         }
       }
     }
@@ -656,269 +682,361 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
 }
 
 
-// ------------------------------------------------ persistent tile loop (m > 128, many tiles)
-// When the output has at least one 128 x 256 tile per SM, one CTA per SM
-// walks tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...  The bulk-copy
-// ring runs continuously across tiles, so the next tile's operands stream in
-// while the current tile's MMAs and epilogue run.
+// ------------------------------------ CTA-pair persistent tile loop (m > 128, many tiles)
+// When the output has at least one 128 x 256 tile per SM, the GEMM runs on
+// CTA pairs (clusters of two): each pair computes 256 x 256 output tiles
+// t = pair, pair + pairs, ... with 256 x 256 x 64 block-scaled MMAs
+// (tcgen05 cta_group::2) that the even CTA issues.  CTA r of a pair holds
+// activation row tile 2·mt + r and weight row tile 2·nt + r of every K block
+// in its shared memory, and accumulator rows [128r, 128r + 128) in its tensor
+// memory.  Per SM this halves the weight bytes that each MMA reads from
+// shared memory and that the bulk copies write there, against a one-CTA
+// 128 x 256 tile, and the freed space deepens the operand ring to three
+// stages of two K blocks (the turnaround of a stage - MMAs done, refill
+// issued, 68 KiB landed - is longer than two stages of MMAs on GB300).  The
+// ring runs continuously across tiles.
 //
-// Measured on GB300, this kernel's pipeline is shaped by three facts: the
-// bulk copies one thread issues are serialized (so each of the three operand
-// streams - activation rows, weight tile 0, weight tile 1 - has its own
-// issuing warp); a tcgen05.cp scale copy stalls the MMA queue for hundreds of
-// cycles (so four scale-factor warps write each row's e8m0 bytes into tensor
-// memory with tcgen05.st instead, one warp per 32-lane quadrant, and the MMA
-// thread issues nothing but MMAs); and a 128 x 128 x 64 block-scaled MMA
-// takes 64 cycles, so every 64-K step issues two N = 128 MMAs into the two
-// halves of the 128 x 256 accumulator.  The accumulator is handed back to the
-// MMA issuer once the epilogue warps have read it into registers
-// (acc_empty); their global stores overlap the next tile's MMAs.
+// Hand-offs: each CTA's copies complete on its own full[s], and its scale
+// warps - which write the stage's e8m0 atoms, read straight from the operand
+// images, into their own CTA's tensor memory once the slot's previous MMAs
+// have completed - arrive on its own sf_full[s].  In the odd CTA a relay
+// thread waits for both and makes one arrival on the even CTA's full[s].
+// The MMA thread's commits arrive on empty[s] and acc_full in both CTAs
+// (multicast).  The epilogue warps read their accumulator rows into
+// registers and arrive on their CTA's acc_empty; in the odd CTA warp 0 then
+// forwards that to the even CTA's acc_empty; their global stores overlap
+// the next tile's MMAs.  Only two kinds of arrival cross between the CTAs,
+// both relaxed (they publish nothing the phases they forward have not
+// already made visible in the odd CTA), and their senders and the MMA thread
+// poll: on GB300 a cluster-scope release arrive stalls the issuing thread
+// while the SM's global stores are in flight, and a suspended try_wait
+// notices a remote arrival late.
 //
-// Warps: 0-3 epilogue, 4-7 scale factors, 8 activation copies (and setup),
-// 9 MMA issuer, 10-11 weight copies.
-struct PCfg {
-  static constexpr int BN = 256;
-  // ring depth and K blocks per stage: two double-block stages keep as many
-  // bytes in flight as four single-block ones, with half as many barrier
-  // hand-offs and MMA commits (each commit costs the tensor pipe ~140 cycles,
-  // measured on GB300)
-  static constexpr int kStages = 2;
-  static constexpr int kSuperK = 2;
-  static constexpr int kThreads = 32 * 12;
-  static constexpr int kBTiles = 2;
-  static constexpr int kABytes = kSuperK * kTileBytes;
-  static constexpr int kBBytes = kBTiles * kSuperK * kTileBytes;
+// Warps: 0-7 epilogue (two per 32-lane quadrant, 128 columns each), 8-11
+// scale factors, 12 activation copies (and setup), 13 tensor memory and MMA
+// issue (the relay in the odd CTA), 14 weight copies.
+struct PairCfg {
+  static constexpr int BN = 256;     // output columns per pair tile (128 weight rows per CTA)
+  static constexpr int kStages = 3;  // ring depth
+  static constexpr int kSuperK = 2;  // K blocks per stage (one bulk copy per operand and stage)
+  static constexpr int kThreads = 32 * 15;
+  static constexpr int kStageOpBytes = kSuperK * kTileBytes;  // one operand, one stage
   static constexpr int kOffA = 0;
-  static constexpr int kOffB = kStages * kABytes;
-  static constexpr int kOffStg = kOffB + kStages * kBBytes;
+  static constexpr int kOffB = kStages * kStageOpBytes;
+  static constexpr int kOffStg = kOffB + kStages * kStageOpBytes;
   // epilogue staging: per warp, 32 rows x 32 columns of bf16 (+8 pad)
   static constexpr int kStgCols = 32;
   static constexpr int kStgPitch = kStgCols + 8;
   static constexpr int kStgWarpBytes = 32 * kStgPitch * 2;
-  static constexpr int kOffBars = kOffStg + 4 * kStgWarpBytes;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kOffBars = kOffStg + kEpiWarps * kStgWarpBytes;
   static constexpr int kNumBars = 3 * kStages + 2;  // full, sf_full, empty per stage; acc_full, acc_empty
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-  static constexpr int kSfColsPerBlock = 8 * (1 + kBTiles);  // per K block: A, B0, B1
+  // per K block: A scales (2 atoms x 4 columns), then per atom the B scales
+  // of both weight row tiles (4 + 4 columns)
+  static constexpr int kSfColsPerBlock = 24;
   static constexpr int kSfColsPerStage = kSuperK * kSfColsPerBlock;
   static constexpr int kTmemCols = 512;
   static_assert(BN + kStages * kSfColsPerStage <= kTmemCols, "tensor memory");
-  static constexpr int kWarpCopyA = 8, kWarpMma = 9, kWarpCopyB0 = 10;
+  static constexpr int kWarpSf0 = 8, kWarpCopyA = 12, kWarpMma = 13, kWarpCopyB = 14;
+  // arrivals on the even CTA's barriers
+  static constexpr int kFullArrivals = 3;                      // own A and B copies, the odd CTA's relay
+  static constexpr int kSfArrivals = 4;                        // the CTA's four scale warps
+  static constexpr int kAccEmptyArrivals = kEpiWarps + 1;      // own epilogue warps, the odd CTA's forward
 };
 
-__global__ void __launch_bounds__(PCfg::kThreads, 1)
-    gemm_persistent_kernel(const GemmArgs args, int64_t tiles_m, int64_t tiles_n) {
-  using P = PCfg;
+__global__ void __launch_bounds__(PairCfg::kThreads, 1)
+    gemm_pair_kernel(const GemmArgs args, int64_t tiles_m, int64_t tiles_n) {
+  // tiles_m: 256-row pair tiles of C; tiles_n: 256-column tiles of C
+  using P = PairCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P::kOffBars);  // operand bytes landed
-  uint64_t* sf_full = full + P::kStages;                                 // scales written to tensor memory
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P::kOffBars);  // operand bytes landed (even: both CTAs')
+  uint64_t* sf_full = full + P::kStages;                                 // the CTA's scales written
   uint64_t* empty = sf_full + P::kStages;                                // MMAs done with the stage
-  uint64_t* acc_full = empty + P::kStages;
-  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* acc_full = empty + P::kStages;                               // accumulator complete
+  uint64_t* acc_empty = acc_full + 1;                                    // read out (even: by both CTAs)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P::kOffMisc + 4);
 
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its peer
+  const int64_t pair = blockIdx.x >> 1, pairs = gridDim.x >> 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t KT = args.kt_count;
   const int64_t total = tiles_m * tiles_n;
   const int nss = (int)ceil_div(KT, P::kSuperK);  // stages per tile
+  const int64_t a_row_tiles = ceil_div(args.m, kTileRows);
   const int64_t b_row_tiles = ceil_div(args.b_rows, kTileRows);
   auto stage_kblocks = [&](int ss) -> int {
     const int64_t left = KT - (int64_t)ss * P::kSuperK;
     return left < P::kSuperK ? (int)left : P::kSuperK;
   };
-  // stream 0 = activation rows, streams 1, 2 = weight tiles; one issuing warp each
-  auto issue_stream = [&](int stream, int64_t tile, int ss, int s) {
-    const uint32_t bytes = (uint32_t)stage_kblocks(ss) * kTileBytes;
-    if (stream == 0) {
-      mbar_arrive_expect_tx(&full[s], bytes);
-      bulk_load(smem + P::kOffA + s * P::kABytes, args.a_img + image_block(tile % tiles_m, (int64_t)ss * P::kSuperK, KT),
-                bytes, &full[s]);
-    } else {
-      const int t = stream - 1;
-      const int64_t brt = (tile / tiles_m) * P::kBTiles + t;
-      if (brt >= b_row_tiles) {  // ragged last column tile: nothing to copy
-        mbar_arrive(&full[s]);
-        return;
-      }
-      mbar_arrive_expect_tx(&full[s], bytes);
-      bulk_load(smem + P::kOffB + s * P::kBBytes + t * P::kSuperK * kTileBytes,
-                args.b_img + image_block(brt, (int64_t)ss * P::kSuperK, KT), bytes, &full[s]);
-    }
-  };
+  // a barrier of the even CTA, addressed from either CTA of the pair
+  auto even_bar = [&](uint64_t* bar) -> uint32_t { return map_cluster(smem_addr(bar), 0); };
 
   if (threadIdx.x == P::kWarpCopyA * 32) {
     for (int s = 0; s < P::kStages; ++s) {
-      mbar_init(&full[s], 3);     // one arrival per copy stream
-      mbar_init(&sf_full[s], 4);  // one arrival per scale-factor warp
+      mbar_init(&full[s], rank == 0 ? P::kFullArrivals : 2);
+      mbar_init(&sf_full[s], P::kSfArrivals);
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4);  // one arrival per epilogue warp
+    mbar_init(acc_empty, rank == 0 ? P::kAccEmptyArrivals : P::kEpiWarps);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == P::kWarpMma) {
-    tmem_alloc(tmem_slot, P::kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, P::kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // both CTAs' barriers initialised and tensor memory allocated
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == P::kWarpCopyA || warp >= P::kWarpCopyB0) {
+  if (warp == P::kWarpCopyA || warp == P::kWarpCopyB) {
     // ------------------------------------------------ bulk-copy producers
-    const int stream = warp == P::kWarpCopyA ? 0 : warp - P::kWarpCopyB0 + 1;
-    if (lane == 0 && blockIdx.x < total) {
+    const bool act = warp == P::kWarpCopyA;
+    if (lane == 0) {
       // The activation image is written by the preceding kernel: its stream
-      // waits for that kernel; the weight streams start at once.
-      if (stream == 0) pdl_wait();
+      // waits for that kernel; the weight stream starts at once.
+      if (act) pdl_wait();
+      const uint8_t* img = act ? args.a_img : args.b_img;
+      uint8_t* ring = smem + (act ? P::kOffA : P::kOffB);
       int64_t g = 0;  // stages issued so far
-      for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        bool stop = false;
+      int s = 0;      // its slot
+      uint32_t ph = 0;
+      bool stop = false;
+      for (int64_t tile = pair; tile < total && !stop; tile += pairs) {
+        const int64_t rt = (act ? tile % tiles_m : tile / tiles_m) * 2 + rank;
+        const bool present = rt < (act ? a_row_tiles : b_row_tiles);  // ragged last tile: nothing to copy
         for (int ss = 0; ss < nss; ++ss, ++g) {
-          const int s = (int)(g % P::kStages);
-          if (!wait_bounded(&empty[s], (uint32_t)(((g / P::kStages) & 1) ^ 1), abort_flag)) {
+          if (!wait_bounded(&empty[s], ph ^ 1, abort_flag)) {
             stop = true;
             break;
           }
-          issue_stream(stream, tile, ss, s);
-        }
-        if (stop) break;
-      }
-      if (*abort_flag) {  // let copies already in flight land before the CTA exits
-        for (int s = 0; s < P::kStages && s < g; ++s)
-          wait_bounded(&full[s], (uint32_t)(((g - 1 - s) / P::kStages) & 1), abort_flag, kDrainLimitCycles);
-      }
-    }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------- scale factors into tensor memory
-    // The same column contents tcgen05.cp.32x128b.warpx4 would produce: lane
-    // l of every 32-lane quadrant holds the 16 bytes of atom row l in 4
-    // columns (row groups l, l+32, l+64, l+96; K blocks 0-3), then the 16
-    // bytes of the second atom (K blocks 4-7) in the next 4 columns.  Warp q
-    // writes quadrant q, 8 columns per operand and K block.
-    const int quad = warp - 4;
-    int64_t g = 0;
-    for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      bool stop = false;
-      for (int ss = 0; ss < nss; ++ss, ++g) {
-        const int s = (int)(g % P::kStages);
-        if (!__all_sync(0xFFFFFFFFu, wait_bounded(&full[s], (uint32_t)((g / P::kStages) & 1), abort_flag))) {
-          stop = true;
-          break;
-        }
-        const int cnt = stage_kblocks(ss);
-        for (int j = 0; j < P::kSuperK; ++j) {
-          if (j >= cnt) break;
-          const uint8_t* sf_src[3] = {smem + P::kOffA + s * P::kABytes + j * kTileBytes + kTileDataBytes,
-                                      smem + P::kOffB + s * P::kBBytes + j * kTileBytes + kTileDataBytes,
-                                      smem + P::kOffB + s * P::kBBytes + (P::kSuperK + j) * kTileBytes + kTileDataBytes};
-#pragma unroll
-          for (int o = 0; o < 3; ++o) {
-            const uint4 lo = *reinterpret_cast<const uint4*>(sf_src[o] + lane * 16);
-            const uint4 hi = *reinterpret_cast<const uint4*>(sf_src[o] + kAtomBytes + lane * 16);
-            const uint32_t v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-            const uint32_t col = P::BN + s * P::kSfColsPerStage + j * P::kSfColsPerBlock + o * 8;
-            tmem_store_8(tmem + ((uint32_t)(quad * 32) << 16) + col, v);
+          if (present) {
+            const uint32_t bytes = (uint32_t)stage_kblocks(ss) * kTileBytes;
+            mbar_arrive_expect_tx(&full[s], bytes);
+            bulk_load(ring + s * P::kStageOpBytes, img + image_block(rt, (int64_t)ss * P::kSuperK, KT), bytes, &full[s]);
+          } else {
+            mbar_arrive(&full[s]);
+          }
+          if (++s == P::kStages) {
+            s = 0;
+            ph ^= 1;
           }
         }
-        tmem_store_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sf_full[s]);
       }
-      if (stop) break;
+      if (act && !stop) {
+        // The MMA thread's commits arrive on empty[] in both CTAs; the last
+        // ones must have landed before this CTA may exit.
+        for (int64_t q = g > P::kStages ? g - P::kStages : 0; q < g; ++q)
+          wait_bounded(&empty[q % P::kStages], (uint32_t)((q / P::kStages) & 1), abort_flag, kDrainLimitCycles);
+      }
+      if (*abort_flag) {  // let copies already in flight land before the CTA exits
+        for (int64_t q = g > P::kStages ? g - P::kStages : 0; q < g; ++q)
+          drain_wait(&full[q % P::kStages], (uint32_t)((q / P::kStages) & 1));
+      }
+    }
+    __syncwarp();
+  } else if (warp >= P::kWarpSf0 && warp < P::kWarpSf0 + 4) {
+    // ------------------------------------- scale factors into tensor memory
+    // Lane l of every 32-lane quadrant holds the 16 bytes of atom row l of an
+    // operand block in 4 columns (row groups l, l+32, l+64, l+96; K blocks
+    // 0-3), the content tcgen05.cp.32x128b.warpx4 would produce.  Per K
+    // block: the A atoms (columns 0-7), then for each atom the two weight row
+    // tiles' atoms side by side (8-15, 16-23), which is the 256-row B-scale
+    // layout of the pair MMA.  Warp 8 + q writes quadrant q.  The atoms come
+    // straight from the operand images: the next stage's loads are in flight
+    // while the warp waits for the slot to free.
+    const int quad = warp - P::kWarpSf0;
+    pdl_wait();  // the activation image is written by the preceding kernel
+    uint4 sfv[P::kSuperK][3][2];  // [K block][A, B0, B1][atom]
+    auto load_stage = [&](int64_t tile, int ss) {
+#pragma unroll
+      for (int j = 0; j < P::kSuperK; ++j) {
+        const int64_t kt = (int64_t)ss * P::kSuperK + j;
+        if (kt >= KT) break;
+        const uint8_t* src[3];
+        const int64_t art = (tile % tiles_m) * 2 + rank;
+        src[0] = art < a_row_tiles ? args.a_img + image_block(art, kt, KT) + kTileDataBytes : nullptr;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int64_t brt = (tile / tiles_m) * 2 + t;
+          src[1 + t] = brt < b_row_tiles ? args.b_img + image_block(brt, kt, KT) + kTileDataBytes : nullptr;
+        }
+        // a missing row tile (ragged edge) gets zero scales; its rows are never stored
+#pragma unroll
+        for (int o = 0; o < 3; ++o) {
+          sfv[j][o][0] = src[o] ? ldg_nc_v4(src[o] + lane * 16) : make_uint4(0, 0, 0, 0);
+          sfv[j][o][1] = src[o] ? ldg_nc_v4(src[o] + kAtomBytes + lane * 16) : make_uint4(0, 0, 0, 0);
+        }
+      }
+    };
+    int64_t tile = pair;
+    int ss = 0, s = 0;
+    uint32_t ph = 0;
+    if (tile < total) load_stage(tile, 0);
+    while (tile < total) {
+      // tensor-memory slot s is free once the MMAs of its previous stage completed
+      if (!__all_sync(0xFFFFFFFFu, wait_bounded(&empty[s], ph ^ 1, abort_flag))) break;
+      tc_fence_after();
+      const int cnt = stage_kblocks(ss);
+#pragma unroll
+      for (int j = 0; j < P::kSuperK; ++j) {
+        if (j >= cnt) break;
+        const uint32_t col = tmem + ((uint32_t)(quad * 32) << 16) + P::BN + s * P::kSfColsPerStage + j * P::kSfColsPerBlock;
+        const uint4 a0 = sfv[j][0][0], a1 = sfv[j][0][1];
+        const uint4 b00 = sfv[j][1][0], b01 = sfv[j][1][1], b10 = sfv[j][2][0], b11 = sfv[j][2][1];
+        const uint32_t va[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const uint32_t vb0[8] = {b00.x, b00.y, b00.z, b00.w, b10.x, b10.y, b10.z, b10.w};
+        const uint32_t vb1[8] = {b01.x, b01.y, b01.z, b01.w, b11.x, b11.y, b11.z, b11.w};
+        tmem_store_8(col, va);
+        tmem_store_8(col + 8, vb0);
+        tmem_store_8(col + 16, vb1);
+      }
+      tmem_store_wait();  // the source registers are reused below
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sf_full[s]);
+      if (++s == P::kStages) {
+        s = 0;
+        ph ^= 1;
+      }
+      if (++ss == nss) {
+        ss = 0;
+        tile += pairs;
+      }
+      if (tile < total) load_stage(tile, ss);  // the next stage's atoms, in flight during the next wait
     }
   } else if (warp == P::kWarpMma) {
-    // ------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int64_t g = 0;
-      uint32_t it = 0;
-      for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-        if (!wait_bounded(acc_empty, (it & 1) ^ 1, abort_flag)) break;  // previous tile drained
-        tc_fence_after();
-        bool aborted = false;
-        bool accumulate = false;
-        for (int ss = 0; ss < nss; ++ss, ++g) {
-          const int s = (int)(g % P::kStages);
-          const uint32_t ph = (uint32_t)((g / P::kStages) & 1);
-          if (!wait_bounded(&full[s], ph, abort_flag) || !wait_bounded(&sf_full[s], ph, abort_flag)) {
+    if (rank == 1) {
+      // ---------------------------------------------------- relay (odd CTA)
+      // forwards "this CTA's operand bytes and scales of stage g are in
+      // place" to the even CTA, whose MMAs read them
+      if (lane == 0) {
+        int s = 0;
+        uint32_t ph = 0;
+        bool stop = false;
+        for (int64_t tile = pair; tile < total && !stop; tile += pairs) {
+          for (int ss = 0; ss < nss; ++ss) {
+            if (!wait_bounded_poll(&full[s], ph, abort_flag) || !wait_bounded_poll(&sf_full[s], ph, abort_flag)) {
+              stop = true;
+              break;
+            }
+            // Relaxed: the bytes and scales are in place once both phases
+            // completed, and a cluster-scope release arrive was measured to
+            // stall this thread 0.5-1.2 us on GB300 while the epilogue's
+            // stores are in flight.
+            mbar_arrive_remote_relaxed(even_bar(&full[s]));
+            if (++s == P::kStages) {
+              s = 0;
+              ph ^= 1;
+            }
+          }
+        }
+      }
+    } else if (lane == 0) {
+      // ------------------------------------------------ MMA issuer (even CTA)
+      // The MMA queue is shallow: whatever this thread does between two
+      // stages' MMAs shows as idle tensor pipe, so the per-stage work is a
+      // few integer adds: descriptors are a base plus the block's offset in
+      // 16-byte units (shared addresses stay below 2^18, inside the
+      // descriptor's 14-bit field), slot and phase are small counters,
+      // never a 64-bit division.
+      const uint32_t ie = idesc_mxf4(256, 256, 0, 0), io = idesc_mxf4(256, 256, 2, 2);
+      const uint64_t adesc0 = smem_desc(smem_addr(smem + P::kOffA), 0, 1024, kLayoutSwizzle128);
+      const uint64_t bdesc0 = smem_desc(smem_addr(smem + P::kOffB), 0, 1024, kLayoutSwizzle128);
+      const int64_t kt_whole = args.k / kTileK;  // K blocks with all four 64-K steps
+      int s = 0;
+      uint32_t ph = 0, it = 0;
+      bool aborted = false;
+      for (int64_t tile = pair; tile < total && !aborted; tile += pairs, ++it) {
+        if (!wait_bounded_poll(acc_empty, (it & 1) ^ 1, abort_flag)) break;  // previous tile read out
+        for (int ss = 0; ss < nss; ++ss) {
+          if (!wait_bounded_poll(&full[s], ph, abort_flag) || !wait_bounded_poll(&sf_full[s], ph, abort_flag)) {
             aborted = true;
             break;
           }
           tc_fence_after();
           const int cnt = stage_kblocks(ss);
-          for (int j = 0; j < cnt; ++j) {
-            const uint32_t a_blk = smem_addr(smem + P::kOffA + s * P::kABytes + j * kTileBytes);
-            const uint32_t b0 = smem_addr(smem + P::kOffB + s * P::kBBytes + j * kTileBytes);
-            const uint32_t b1 = b0 + P::kSuperK * kTileBytes;
+#pragma unroll
+          for (int j = 0; j < P::kSuperK; ++j) {
+            if (j >= cnt) break;
             const uint32_t sf = tmem + P::BN + s * P::kSfColsPerStage + j * P::kSfColsPerBlock;
-            const uint64_t ad = smem_desc(a_blk, 0, 1024, kLayoutSwizzle128);
-            const uint64_t bd0 = smem_desc(b0, 0, 1024, kLayoutSwizzle128);
-            const uint64_t bd1 = smem_desc(b1, 0, 1024, kLayoutSwizzle128);
-            const int steps = k_steps(args.k, (int64_t)ss * P::kSuperK + j);
-            if (steps == 4) {  // a whole K block: its eight MMAs in one go
-              mma_mxf4_kblock_n256(tmem, ad, bd0, bd1, idesc_mxf4(128, 128, 0, 0), idesc_mxf4(128, 128, 2, 2), sf,
-                                   sf + 8, sf + 16, accumulate ? 1u : 0u);
-              accumulate = true;
+            const uint32_t acc = (ss > 0 || j > 0) ? 1u : 0u;
+            const int64_t kt = (int64_t)ss * P::kSuperK + j;
+            const uint64_t off = (uint64_t)((s * P::kStageOpBytes + j * kTileBytes) >> 4);
+            const uint64_t ad = adesc0 + off, bd = bdesc0 + off;
+            if (kt < kt_whole) {  // a whole K block: its four MMAs in one go
+              mma_mxf4_pair_kblock(tmem, ad, bd, ie, io, sf, sf + 8, acc);
             } else {
+              const int steps = k_steps(args.k, kt);
               for (int kk = 0; kk < steps; ++kk) {
                 // advancing the start address by 32 bytes = 2 in the descriptor's 16-byte units
                 const uint64_t adv = (uint64_t)(kk * 2);
-                const uint32_t id = (uint32_t)(kk & 1) * 2;
-                const uint32_t acc = accumulate ? 1u : 0u;
-                const uint32_t sfk = (uint32_t)(kk >> 1) * 4;
-                mma_mxf4(tmem, ad + adv, bd0 + adv, idesc_mxf4(128, 128, id, id), sf + sfk, sf + 8 + sfk, acc);
-                mma_mxf4(tmem + 128, ad + adv, bd1 + adv, idesc_mxf4(128, 128, id, id), sf + sfk, sf + 16 + sfk,
-                         acc);
-                accumulate = true;
+                mma_mxf4_pair(tmem, ad + adv, bd + adv, (kk & 1) ? io : ie,
+                              sf + (uint32_t)(kk >> 1) * 4, sf + 8 + (uint32_t)(kk >> 1) * 8, (acc || kk > 0) ? 1u : 0u);
               }
             }
           }
-          mma_commit(&empty[s]);
+          mma_commit_pair(&empty[s], 0x3);
+          if (++s == P::kStages) {
+            s = 0;
+            ph ^= 1;
+          }
         }
-        mma_commit(acc_full);  // fires when this tile's MMAs have completed
-        if (aborted) break;
+        mma_commit_pair(acc_full, 0x3);  // fires when this tile's MMAs have completed
       }
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // --------------------------------------------- epilogue (warps 0-3)
-    // The whole 32 x 256 slice of the accumulator is read into registers as
-    // packed bf16 (128 registers) before the accumulator is handed back, so
-    // the next tile's MMAs wait only for the tensor-memory reads, not for
-    // the global stores.
-    const int quad = warp;
+  } else if (warp < P::kEpiWarps) {
+    // --------------------------------------------- epilogue (warps 0-7)
+    // This CTA's 128 accumulator rows: warp w reads the 32 x 128 slice of
+    // quadrant w % 4 and column half w / 4 into registers as packed bf16 (64
+    // registers) and hands the accumulator back before storing, so the next
+    // tile's MMAs wait only for the tensor-memory reads, not for the global
+    // stores.
+    constexpr int kCols = P::BN / 2;
+    const int quad = warp % 4, half = warp / 4;
     __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem + P::kOffStg + warp * P::kStgWarpBytes);
     uint32_t it = 0;
-    for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      const int64_t m0 = (tile % tiles_m) * kTileRows + quad * 32;
-      const int64_t n0 = (tile / tiles_m) * P::BN;
-      const bool ok = wait_bounded(acc_full, it & 1, abort_flag);
+    for (int64_t tile = pair; tile < total; tile += pairs, ++it) {
+      const bool ok = wait_bounded_poll(acc_full, it & 1, abort_flag);
       tc_fence_after();
-      uint32_t packed[P::BN / 16][8];
+      uint32_t packed[kCols / 16][8];
 #pragma unroll
-      for (int c = 0; c < P::BN / 16; ++c) {
-        uint32_t r[16];
-        tmem_load_16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(c * 16), r);
+      for (int c = 0; c < kCols / 16; c += 2) {  // two loads in flight per wait
+        uint32_t r[2][16];
+        tmem_load_16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * kCols + c * 16), r[0]);
+        tmem_load_16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * kCols + c * 16 + 16), r[1]);
         tmem_load_wait();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) packed[c][j] = bf16x2_bits(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            packed[c + u][j] = bf16x2_bits(__uint_as_float(r[u][2 * j]), __uint_as_float(r[u][2 * j + 1]));
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);  // accumulator free for the next tile
+      if (lane == 0) mbar_arrive(acc_empty);  // accumulator rows read out: free for the next tile
+      if (rank == 1 && warp == 0 && lane == 0) {
+        // Forward once all eight have arrived.  The reads have completed
+        // (tcgen05.wait::ld), nothing is published: a relaxed arrival, which
+        // does not wait for this thread's stores of the previous tile.
+        if (wait_bounded_poll(acc_empty, it & 1, abort_flag)) mbar_arrive_remote_relaxed(even_bar(acc_empty));
+      }
       if (!ok) continue;
+      const int64_t m0 = (tile % tiles_m) * (2 * kTileRows) + rank * kTileRows + quad * 32;
+      const int64_t n0 = (tile / tiles_m) * P::BN + half * kCols;
       // 32-column chunks through the warp's staging slice: each lane writes
       // its row's 64 bytes, then every store instruction covers eight 64-byte
-      // row segments (few, wide transactions for the LSU, which the
-      // scale-factor warps' shared loads share)
+      // row segments (few, wide transactions for the LSU)
 #pragma unroll
-      for (int cc = 0; cc < P::BN / P::kStgCols; ++cc) {
+      for (int cc = 0; cc < kCols / P::kStgCols; ++cc) {
         uint4* row_dst = reinterpret_cast<uint4*>(stg + lane * P::kStgPitch);
 #pragma unroll
         for (int q = 0; q < P::kStgCols / 8; ++q) {
@@ -947,11 +1065,14 @@ __global__ void __launch_bounds__(PCfg::kThreads, 1)
     }
   }
 
+  // Neither CTA frees its tensor memory or exits while the pair still needs
+  // it: every MMA has completed (both epilogues waited for the last
+  // accumulator), every remote arrival has been made.
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == P::kWarpMma) {
     tc_fence_after();
-    tmem_dealloc(tmem, P::kTmemCols);
+    tmem_dealloc_pair(tmem, P::kTmemCols);
   }
 }
 
@@ -1012,9 +1133,10 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan, bool a_image
     p.split = s;
     p.grid_y = nt * s;
     p.workspace = a_image ? 0 : (size_t)image_bytes(m, k);
-    if (p.bn == 256) {  // at least one 128 x 256 tile per SM: persistent tile loop
+    if (p.bn == 256) {  // at least one 128 x 256 tile per SM: CTA pairs loop over 256 x 256 tiles
       p.persistent = true;
-      p.grid_x = mt * nt < sms ? mt * nt : sms;
+      const int64_t pair_tiles = ceil_div(m, 2 * kTileRows) * nt;
+      p.grid_x = 2 * (pair_tiles < sms / 2 ? pair_tiles : sms / 2);
       p.grid_y = 1;
     }
   }
@@ -1103,28 +1225,63 @@ static cudaError_t launch_one(const GemmPlan& plan_in, const GemmArgs& args_in, 
   return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, kMode>, args);
 }
 
-static cudaError_t launch_persistent(const GemmPlan& plan, const GemmArgs& args, int64_t tiles_m, int64_t tiles_n,
-                                     cudaStream_t stream) {
+// CTA pairs of the pair kernel that can be resident at once (cached per device).
+static int max_resident_pairs() {
+  static int cache[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(PairCfg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = PairCfg::kSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();  // clear the error: the launch decides
+      n = -1;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+static cudaError_t launch_pair(const GemmPlan& plan, const GemmArgs& args, int64_t tiles_m, int64_t tiles_n,
+                               cudaStream_t stream) {
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
     cudaError_t e =
-        cudaFuncSetAttribute(gemm_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg::kSmemBytes);
+        cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
+  int64_t pairs = plan.grid_x / 2;
+  const int resident = max_resident_pairs();
+  if (resident > 0 && pairs > resident) pairs = resident;  // one wave: every pair loops over its tiles
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((unsigned)plan.grid_x, 1, 1);
-  cfg.blockDim = dim3(PCfg::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = PCfg::kSmemBytes;
+  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(PairCfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = PairCfg::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;  // dependent of the quantization kernel
-  attr.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_persistent_kernel, args, tiles_m, tiles_n);
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 2;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // dependent of the quantization kernel
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel, args, tiles_m, tiles_n);
 }
 
 cudaError_t launch_gemm(const GemmPlan& plan, const void* a_bf16, int64_t m, int64_t k, int64_t lda,
@@ -1171,7 +1328,7 @@ cudaError_t launch_gemm(const GemmPlan& plan, const void* a_bf16, int64_t m, int
   args.a_img = static_cast<const uint8_t*>(a_image);
   args.b_img = static_cast<const uint8_t*>(b_image);
   args.b_rows = n;
-  if (plan.persistent) return launch_persistent(plan, args, ceil_div(m, kTileRows), ceil_div(n, PCfg::BN), stream);
+  if (plan.persistent) return launch_pair(plan, args, ceil_div(m, 2 * kTileRows), ceil_div(n, PairCfg::BN), stream);
   switch (plan.bn) {
     case 128: return launch_one<128, kImagePlain>(plan, args, stream);
     default: return cudaErrorInvalidValue;

@@ -29,7 +29,7 @@ struct GemmPlan {
   bool swap_ab;        // weights on the MMA's 128-row side
   int bn;              // MMA N: padded m (swap) or the n tile (no swap)
   int split;           // CTAs per cluster splitting K
-  bool persistent;     // one CTA per SM looping over 128 x 256 tiles (plain mode, many tiles)
+  bool persistent;     // CTA pairs (one per two SMs) looping over 256 x 256 tiles (plain mode, many tiles)
   int64_t grid_x;      // 128-row tiles of the MMA-A operand
   int64_t grid_y;      // N tiles times split
   size_t workspace;    // bytes of caller workspace the plan needs

@@ -156,6 +156,68 @@ __device__ __forceinline__ void mma_mxf4_kblock_n256(uint32_t d, uint64_t a, uin
       : "memory");
 }
 
+// ---------------------------------------------- CTA-pair (cta_group::2) forms
+// Tensor memory of a CTA pair is allocated, released and freed collectively:
+// one warp of each of the two CTAs executes the instruction, and both CTAs
+// receive the same base address (measured on GB300).  A kernel uses either
+// these forms or the cta_group::1 ones, never both.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// One K = 64 step of a 256 x N pair MMA, issued by one thread of the even
+// CTA: rows 0-127 of A and D live in the even CTA (its shared memory and
+// tensor memory), rows 128-255 in the odd one, at the same addresses; B's
+// first N/2 rows come from the even CTA's shared memory, the rest from the
+// odd CTA's.  Scales: each CTA's tensor memory holds the A scales of its own
+// 128 rows (row r at lane r, column r/32) and the B scales of all N rows
+// (row j at column j/32, lane j mod 32 of every 32-lane quadrant) - the
+// placement measured on GB300.
+__device__ __forceinline__ void mma_mxf4_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                              uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// The four K = 64 steps of one 256-K block of a 256 x 256 pair MMA, from one
+// asm block.  A scales advance 4 columns per two steps (128 rows per atom),
+// B scales 8 (256 rows).
+__device__ __forceinline__ void mma_mxf4_pair_kblock(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc_even,
+                                                     uint32_t idesc_odd, uint32_t sfa, uint32_t sfb,
+                                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, a2, a3, c1, c2, c3;\n\t.reg .b32 sa1, sb1;\n\t"
+      "setp.ne.b32 p, %7, 0;\n\tsetp.eq.b32 q, %7, %7;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+      "add.s64 c1, %2, 2;\n\tadd.s64 c2, %2, 4;\n\tadd.s64 c3, %2, 6;\n\t"
+      "add.u32 sa1, %5, 4;\n\tadd.u32 sb1, %6, 8;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], a1, c1, %4, [%5], [%6], q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], a2, c2, %3, [sa1], [sb1], q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], a3, c3, %4, [sa1], [sb1], q;\n\t}"
+      ::"r"(d), "l"(a), "l"(b), "r"(idesc_even), "r"(idesc_odd), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the mbarrier at `bar`'s offset in each CTA of `cta_mask`
+// when every tcgen05 operation this thread issued before it has completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued
 // before it has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -230,12 +292,38 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Arrive on an mbarrier of another CTA of the cluster (address from
+// map_cluster), releasing this thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_caddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_caddr) : "memory");
+}
+// The same arrival without release semantics: for hand-offs that publish no
+// memory (say, "these tensor-memory reads have completed"), so the thread
+// need not wait for its earlier global stores to be performed first.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t bar_caddr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_caddr) : "memory");
+}
 // try_wait that acquires writes released at cluster scope by other CTAs.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Non-blocking test of a phase, acquiring at cluster scope.  A thread that
+// polls with it sees an arrival from another CTA as soon as it lands; a
+// try_wait that suspended the thread was measured on GB300 to resume some
+// 0.5-1 us after such an arrival.
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_addr(bar)), "r"(parity)

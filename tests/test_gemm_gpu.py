@@ -224,13 +224,28 @@ def test_quant_image_then_gemm_image(m, n, k):
 
 def test_persistent_tile_loop_with_ragged_tails():
     """m=1000, n=4856, k=544: 8 x 19 = 152 output tiles of 128 x 256 (at least one
-    per SM) run through the persistent tile loop; the last row tile, the last
-    column tile (248 of 256 columns, the second weight tile partial) and the
-    last K tile (32 of 256) are all ragged, and some CTAs take two tiles."""
+    per SM) run on the CTA-pair kernel as 4 x 19 tiles of 256 x 256; the last
+    row tile (104 rows in the odd CTA), the last column tile (248 of 256
+    columns, the second weight tile partial) and the last K tile (32 of 256)
+    are all ragged."""
     m, n, k = 1000, 4856, 544
     a = inputs.random_bf16(m, k, seed=77)
     b = inputs.random_bf16(n, k, seed=78, std=0.2)
     packed, bq, bs = packed_from_oracle(b)
     got, c_full = _run(a, packed, ldc=n + 8)
     assert_close_to_ref(got, _oracle_full(a, bq, bs), what="persistent")
+    assert torch.isnan(c_full[:, n:]).all()
+
+
+def test_pair_kernel_more_tiles_than_pairs_and_missing_row_tile():
+    """m=1100, n=4856, k=800: 5 x 19 = 95 tiles of 256 x 256 on the CTA pairs,
+    so some pairs take two tiles and the ring runs across tiles; the last row
+    tile pair has rows 1024-1099 in the even CTA and no activation rows at all
+    in the odd one; the last stage holds one and a bit K blocks (K tail 32)."""
+    m, n, k = 1100, 4856, 800
+    a = inputs.random_bf16(m, k, seed=91)
+    b = inputs.random_bf16(n, k, seed=92, std=0.2)
+    packed, bq, bs = packed_from_oracle(b)
+    got, c_full = _run(a, packed, ldc=n + 8)
+    assert_close_to_ref(got, _oracle_full(a, bq, bs), what="pair kernel, 95 tiles")
     assert torch.isnan(c_full[:, n:]).all()
