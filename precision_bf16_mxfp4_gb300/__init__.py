@@ -131,7 +131,10 @@ class ActImage:
 
 
 def quant_image(a, out=None) -> ActImage:
-    """bf16 A [m,k] CUDA tensor -> ActImage (MXFP4, operand layout)."""
+    """bf16 A [m,k] CUDA tensor -> ActImage (MXFP4, operand layout).
+
+    `out` (optional) is the image buffer to overwrite: an ActImage of the same
+    (m, k) or a uint8 device tensor of at least act_image_bytes(m, k) bytes."""
     torch = _torch()
     _require_cuda(a, "a")
     if a.dtype != torch.bfloat16 or a.dim() != 2 or a.stride(1) != 1:
@@ -140,6 +143,10 @@ def quant_image(a, out=None) -> ActImage:
     nbytes = mxfp4_act_image_bytes(m, k)
     if nbytes == 0:
         raise ValueError("unsupported (m, k)")
+    if isinstance(out, ActImage):
+        if (out.m, out.k) != (m, k):
+            raise ValueError("out is an image of another (m, k)")
+        out = out.buf
     buf = out if out is not None else torch.empty(nbytes, dtype=torch.uint8, device=a.device)
     st = mxfp4_quant_image(ctypes_void(a.data_ptr()), m, k, a.stride(0), ctypes_void(buf.data_ptr()),
                            buf.numel() * buf.element_size(), _stream_handle(a.device))

@@ -134,6 +134,23 @@ __device__ __forceinline__ uint4 quantize_block32(const uint4 (&w)[4], uint32_t&
                     encode8<kHardwareCvt>(w[2], inv), encode8<kHardwareCvt>(w[3], inv));
 }
 
+// One 32-element block held by a quad of lanes (lanes 4j..4j+3, 8 bf16 each
+// in K order, lane 4j first): the same block maximum, scale and codes as
+// quantize_block32, with the maximum reduced across the quad by shuffles.
+// Returns this lane's 4 packed bytes (bytes 4q..4q+3 of the block's 16);
+// every lane of the quad gets the scale byte.  All 32 lanes must call it.
+template <bool kHardwareCvt>
+__device__ __forceinline__ uint32_t quantize_quad(const uint4& w, uint32_t& scale_byte) {
+  constexpr uint32_t kMag = 0x7FFF7FFFu;
+  const uint32_t c = __vmaxu2(__vmaxu2(w.x & kMag, w.y & kMag), __vmaxu2(w.z & kMag, w.w & kMag));
+  uint32_t m = max(c & 0xFFFFu, c >> 16);
+  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+  const int ub = block_exponent(m);
+  scale_byte = (uint32_t)(ub + 127);
+  return encode8<kHardwareCvt>(w, inverse_scale(ub));
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -4,10 +4,8 @@
 //   quant_image_kernel  : bf16 A[m,k] -> tiled operand image (see mxfp4_device.cuh)
 //   prepack_*_kernel    : linear MXFP4 B -> tiled operand image
 //
-// One thread owns one 32-element scale block: it loads the block's 64 bytes,
-// forms the block maximum in registers and writes 16 packed bytes plus the
-// scale byte.  Consecutive threads take consecutive blocks of a row, so a
-// warp reads 2 KiB of contiguous bf16 and writes 512 contiguous bytes.
+// A warp quantizes 256-element row segments (four lanes per 32-element
+// block), reading 512 contiguous bytes per load instruction.
 #include <cuda_runtime.h>
 
 #include "mxfp4_device.cuh"
@@ -17,33 +15,52 @@
 namespace mxfp4 {
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantUnroll = 4;  // blocks in flight per thread
+constexpr int kQuantSegBatch = 4;  // row segments whose loads one warp keeps in flight
 
+// Both quantizers work in row segments: 256 consecutive K elements (8 scale
+// blocks) of one row, one segment per warp.  Lane l holds elements 8l..8l+7
+// (one 16-byte load; the warp reads 512 contiguous bytes), a quad of lanes
+// holds one block, and the block maximum is reduced across the quad.  A warp
+// loads up to kQuantSegBatch segments before quantizing any, so enough bytes
+// are in flight to cover HBM latency with few registers per thread.
+// Segments are dealt round-robin over all warps of the grid.
+
+// seg / d, in 32-bit arithmetic when every segment index of the grid fits
+// (a 64-bit division is a long software sequence on the GPU).
+__device__ __forceinline__ int64_t div_seg(int64_t seg, int64_t d, bool small) {
+  return small ? (int64_t)((uint32_t)seg / (uint32_t)d) : seg / d;
+}
+
+// bf16 A[m,k] -> packed e2m1 [m,k/2] + e8m0 [m,k/32] (k a multiple of 32).
 template <bool kHw>
 __global__ void __launch_bounds__(kQuantThreads)
     quant_linear_kernel(const uint16_t* __restrict__ a, int64_t m, int64_t k, int64_t lda,
                         uint8_t* __restrict__ q, uint8_t* __restrict__ scale) {
-  const int64_t blocks_per_row = k / 32;
-  const int64_t total = m * blocks_per_row;
-  const int64_t nthreads = (int64_t)gridDim.x * kQuantThreads;
-  const int64_t t0 = (int64_t)blockIdx.x * kQuantThreads + threadIdx.x;
-  for (int64_t base = t0; base < total; base += nthreads * kQuantUnroll) {
-    uint4 w[kQuantUnroll][4];
-    int64_t row[kQuantUnroll], blk[kQuantUnroll];
+  const int lane = threadIdx.x & 31;
+  const int64_t segs_per_row = ceil_div(k, kTileK);
+  const int64_t total = m * segs_per_row;
+  const bool small = total + (int64_t)gridDim.x * kQuantThreads * kQuantSegBatch < (1ll << 31);
+  const int64_t warps = (int64_t)gridDim.x * (kQuantThreads / 32);
+  const int64_t w0 = (int64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
+  for (int64_t base = w0; base < total; base += warps * kQuantSegBatch) {
+    uint4 v[kQuantSegBatch];
+    int64_t row[kQuantSegBatch], col[kQuantSegBatch];
 #pragma unroll
-    for (int u = 0; u < kQuantUnroll; ++u) {
-      const int64_t t = base + (int64_t)u * nthreads;
-      row[u] = t / blocks_per_row;
-      blk[u] = t - row[u] * blocks_per_row;
-      if (t < total) ldg_nc_block(a + row[u] * lda + blk[u] * 32, w[u]);
+    for (int i = 0; i < kQuantSegBatch; ++i) {
+      const int64_t seg = base + (int64_t)i * warps;
+      row[i] = div_seg(seg, segs_per_row, small);
+      col[i] = (seg - row[i] * segs_per_row) * kTileK + lane * 8;
+      v[i] = (seg < total && col[i] < k) ? ldg_nc_v4(a + row[i] * lda + col[i]) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int u = 0; u < kQuantUnroll; ++u) {
-      if (base + (int64_t)u * nthreads >= total) continue;
+    for (int i = 0; i < kQuantSegBatch; ++i) {
+      if (base + (int64_t)i * warps >= total) break;  // uniform across the warp
       uint32_t sbyte;
-      const uint4 packed = quantize_block32<kHw>(w[u], sbyte);
-      *reinterpret_cast<uint4*>(q + row[u] * (k / 2) + blk[u] * 16) = packed;
-      scale[row[u] * blocks_per_row + blk[u]] = (uint8_t)sbyte;
+      const uint32_t packed = quantize_quad<kHw>(v[i], sbyte);
+      if (col[i] < k) {
+        *reinterpret_cast<uint32_t*>(q + row[i] * (k / 2) + col[i] / 2) = packed;
+        if ((lane & 3) == 0) scale[row[i] * (k / 32) + col[i] / 32] = (uint8_t)sbyte;
+      }
     }
   }
 }
@@ -52,9 +69,9 @@ __global__ void __launch_bounds__(kQuantThreads)
 // image, rows >= m as zeros (rows_out = m leaves the last row tile's padding
 // rows untouched: an activation's padding rows only reach accumulator rows
 // that are never stored; a weight image needs them zero).  K beyond k up to
-// the tile edge is written as zeros.  Thread t covers block b = t % 8 of K
-// block kt of a row, so eight consecutive threads write one swizzled
-// 128-byte row of a data tile.
+// the tile edge is written as zeros.  A segment is one 128-byte row of a data
+// tile (the warp's 32 four-byte stores fill it, in swizzled chunk order) and
+// two scale words of the tile's atoms.
 template <bool kHw>
 __global__ void __launch_bounds__(kQuantThreads)
     quant_image_kernel(const uint16_t* __restrict__ a, int64_t m, int64_t k, int64_t lda,
@@ -62,37 +79,38 @@ __global__ void __launch_bounds__(kQuantThreads)
   // Let the dependent GEMM launch now: it prefetches weights and waits for
   // this grid's completion before it reads the image.
   pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
   const int64_t kt_count = ceil_div(k, kTileK);
-  const int64_t total = rows_out * kt_count * 8;
-  const int64_t nthreads = (int64_t)gridDim.x * kQuantThreads;
-  const int64_t t0 = (int64_t)blockIdx.x * kQuantThreads + threadIdx.x;
-  for (int64_t base = t0; base < total; base += nthreads * kQuantUnroll) {
-    uint4 w[kQuantUnroll][4];
-    int64_t row[kQuantUnroll], kt[kQuantUnroll];
-    int b[kQuantUnroll];
+  const int64_t total = rows_out * kt_count;
+  const bool small = total + (int64_t)gridDim.x * kQuantThreads * kQuantSegBatch < (1ll << 31);
+  const int64_t warps = (int64_t)gridDim.x * (kQuantThreads / 32);
+  const int64_t w0 = (int64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
+  for (int64_t base = w0; base < total; base += warps * kQuantSegBatch) {
+    uint4 v[kQuantSegBatch];
+    int64_t row[kQuantSegBatch], kt[kQuantSegBatch];
 #pragma unroll
-    for (int u = 0; u < kQuantUnroll; ++u) {
-      const int64_t t = base + (int64_t)u * nthreads;
-      b[u] = (int)(t & 7);
-      row[u] = (t >> 3) / kt_count;
-      kt[u] = (t >> 3) - row[u] * kt_count;
-      const int64_t col = kt[u] * kTileK + b[u] * 32;
-      if (t < total && col < k && row[u] < m) {
-        ldg_nc_block(a + row[u] * lda + col, w[u]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) w[u][i] = make_uint4(0, 0, 0, 0);  // padding: zero codes, scale byte 0
-      }
+    for (int i = 0; i < kQuantSegBatch; ++i) {
+      const int64_t seg = base + (int64_t)i * warps;
+      row[i] = div_seg(seg, kt_count, small);
+      kt[i] = seg - row[i] * kt_count;
+      const int64_t col = kt[i] * kTileK + lane * 8;
+      // padding rows and K: zero codes, scale byte 0
+      v[i] = (seg < total && row[i] < m && col < k) ? ldg_nc_v4(a + row[i] * lda + col) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int u = 0; u < kQuantUnroll; ++u) {
-      if (base + (int64_t)u * nthreads >= total) continue;
+    for (int i = 0; i < kQuantSegBatch; ++i) {
+      if (base + (int64_t)i * warps >= total) break;  // uniform across the warp
       uint32_t sbyte;
-      const uint4 packed = quantize_block32<kHw>(w[u], sbyte);
-      const int r = (int)(row[u] & (kTileRows - 1));
-      uint8_t* tile = img + image_block(row[u] / kTileRows, kt[u], kt_count);
-      *reinterpret_cast<uint4*>(tile + tile_data_offset(r, b[u] * 16)) = packed;
-      tile[kTileDataBytes + tile_sf_offset(r, b[u])] = (uint8_t)sbyte;
+      const uint32_t packed = quantize_quad<kHw>(v[i], sbyte);
+      const int r = (int)(row[i] & (kTileRows - 1));
+      const int b = lane >> 2;
+      uint8_t* tile = img + image_block(row[i] / kTileRows, kt[i], kt_count);
+      *reinterpret_cast<uint32_t*>(tile + tile_data_offset(r, b * 16 + (lane & 3) * 4)) = packed;
+      // scale word of blocks 0-3 (atom 0) and of blocks 4-7 (atom 1): byte b & 3
+      uint32_t word = sbyte << (8 * (b & 3));
+      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 4);
+      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 8);
+      if ((lane & 15) == 0) *reinterpret_cast<uint32_t*>(tile + kTileDataBytes + tile_sf_offset(r, b)) = word;
     }
   }
 }
@@ -143,9 +161,24 @@ static int grid_for(int64_t work_items, int per_block) {
   return (int)blocks;
 }
 
+// Grid of the quantization kernels: one warp per segment up to eight
+// 256-thread CTAs per SM (about two resident waves at these kernels'
+// register counts); beyond that each warp takes several segments, in
+// batches of kQuantSegBatch.  Measured on GB300 the image quantizer of a
+// 4096 x 2048 activation runs about 2 us above a plain copy of the same
+// input: its time goes to the dependent chains of the per-block arithmetic
+// as much as to HBM (a variant staging rows through shared memory with bulk
+// copies, eight warps per SM, was slower).
+static int quant_grid(int64_t segments) {
+  const int64_t max_warps = (int64_t)num_sms() * 8 * (kQuantThreads / 32);
+  const int64_t warps = segments < max_warps ? segments : max_warps;
+  const int64_t blocks = ceil_div(warps, (int64_t)(kQuantThreads / 32));
+  return blocks < 1 ? 1 : (int)blocks;
+}
+
 cudaError_t launch_quant_linear(const void* a, int64_t m, int64_t k, int64_t lda, void* q, void* scale,
                                 cudaStream_t stream) {
-  const int grid = grid_for(m * (k / 32), kQuantThreads);
+  const int grid = quant_grid(m * ceil_div(k, kTileK));
   quant_linear_kernel<kUseHardwareCvt><<<grid, kQuantThreads, 0, stream>>>(
       static_cast<const uint16_t*>(a), m, k, lda, static_cast<uint8_t*>(q), static_cast<uint8_t*>(scale));
   return cudaGetLastError();
@@ -154,7 +187,7 @@ cudaError_t launch_quant_linear(const void* a, int64_t m, int64_t k, int64_t lda
 cudaError_t launch_quant_image(const void* a, int64_t m, int64_t k, int64_t lda, void* img, cudaStream_t stream,
                                bool zero_padding_rows) {
   const int64_t rows_out = zero_padding_rows ? ceil_div(m, kTileRows) * kTileRows : m;
-  const int grid = grid_for(rows_out * ceil_div(k, kTileK) * 8, kQuantThreads);
+  const int grid = quant_grid(rows_out * ceil_div(k, kTileK));
   quant_image_kernel<kUseHardwareCvt><<<grid, kQuantThreads, 0, stream>>>(
       static_cast<const uint16_t*>(a), m, k, lda, static_cast<uint8_t*>(img), rows_out);
   return cudaGetLastError();

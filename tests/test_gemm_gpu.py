@@ -188,11 +188,16 @@ def test_gemm_every_split_factor(m, n, k, split, monkeypatch):
     assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
 
 
-@pytest.mark.parametrize("n,k", [(300, 544), (2880, 512), (129, 288), (2112, 7168)])
-def test_prepack_b_bf16_equals_quant_then_prepack(n, k):
+@pytest.mark.parametrize("n,k,ldb", [(300, 544, 544), (2880, 512, 512), (129, 288, 288), (2112, 7168, 7168),
+                                     (1500, 2336, 2344)])
+def test_prepack_b_bf16_equals_quant_then_prepack(n, k, ldb):
     """The one-call weight path writes the same image bytes as mxfp4_quant
-    followed by mxfp4_prepack_b (padding rows and the K tail zero)."""
-    b = inputs.random_bf16(n, k, seed=n + k, std=0.5).cuda()
+    followed by mxfp4_prepack_b (padding rows and the K tail zero); 1500 x
+    2336 with a row stride of 2344 ends in a K block of 32 and 36 padding
+    rows."""
+    big = torch.full((n, ldb), float("nan"), dtype=torch.bfloat16)
+    big[:, :k] = inputs.random_bf16(n, k, seed=n + k, std=0.5)
+    b = big.cuda()[:, :k]
     one = mx.prepack_b_bf16(b)
     two = mx.prepack_b(*mx.quant(b))
     torch.cuda.synchronize()
@@ -200,7 +205,7 @@ def test_prepack_b_bf16_equals_quant_then_prepack(n, k):
 
 
 @pytest.mark.parametrize("m,n,k", [(4, 2880, 512), (32, 520, 2080), (33, 256, 512), (64, 384, 2048),
-                                   (200, 256, 2048), (1000, 4856, 544)])
+                                   (200, 256, 2048), (1000, 4856, 544), (2044, 512, 2336)])
 def test_quant_image_then_gemm_image(m, n, k):
     """A quantized once into the operand layout, multiplied by two different
     weights: both products match the oracle, and for m > 32 (the same plan
