@@ -75,7 +75,7 @@ struct GemmArgs {
   __nv_bfloat16* c;
   int64_t ldc;
   int split;
-  int drop_copies;  // test hook: issue no bulk copies, so the MMA wait runs out
+  int drop_copies;  // test hook: the MMA issuer's operand wait runs out (see launch_gemm)
 };
 
 template <int BN, int kMode>
@@ -916,8 +916,9 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     if (rank == 1) {
       // ---------------------------------------------------- relay (odd CTA)
       // forwards "this CTA's operand bytes and scales of stage g are in
-      // place" to the even CTA, whose MMAs read them
-      if (lane == 0) {
+      // place" to the even CTA, whose MMAs read them (the test hook forwards
+      // nothing)
+      if (lane == 0 && !args.drop_copies) {
         int s = 0;
         uint32_t ph = 0;
         bool stop = false;
@@ -1297,10 +1298,11 @@ cudaError_t launch_gemm(const GemmPlan& plan, const void* a_bf16, int64_t m, int
   args.split = plan.split;
   args.lda = lda;
   // MXFP4_DEBUG_DROP_COPIES=1 exercises the bounded waits from the tests: the
-  // generic GEMM issues no bulk copies, its MMA wait runs out after about a
-  // second, the kernel sets the device timeout flag and exits normally.
+  // generic GEMM issues no bulk copies, the CTA-pair GEMM's relay forwards
+  // nothing; either way the MMA issuer's wait runs out after about a second,
+  // the kernel sets the device timeout flag, winds down and exits normally.
   const char* drop = getenv("MXFP4_DEBUG_DROP_COPIES");
-  args.drop_copies = (drop && drop[0] == '1' && !plan.persistent) ? 1 : 0;
+  args.drop_copies = (drop && drop[0] == '1') ? 1 : 0;
   if (plan.mode == kFusedSwap) {
     args.a_img = static_cast<const uint8_t*>(b_image);
     args.act = static_cast<const uint16_t*>(a_bf16);

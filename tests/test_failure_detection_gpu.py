@@ -1,7 +1,8 @@
 """Failure detection without a GPU fault: every pipeline wait in the GEMM is
-bounded.  With MXFP4_DEBUG_DROP_COPIES=1 the kernel issues no bulk copies, so
-the MMA issuer's wait for its first stage runs out (about a second); the
-kernel raises the device-side timeout flag and returns normally.  The host
+bounded.  With MXFP4_DEBUG_DROP_COPIES=1 the generic kernel issues no bulk
+copies (the CTA-pair kernel's relay forwards nothing), so the MMA issuer's
+wait for its first stage runs out (about a second); the kernel raises the
+device-side timeout flag and returns normally.  The host
 reads MXFP4_ERR_TIMEOUT from mxfp4_device_status, and the context stays
 usable: the next call computes the right result."""
 from __future__ import annotations
@@ -19,9 +20,13 @@ from tests.helpers import bf16_bits
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("m,split", [(8, "1"), (16, "4"), (48, "2")])
-def test_wait_timeout_is_reported_and_recoverable(m, split, monkeypatch):
-    n, k = 256, 1024
+@pytest.mark.parametrize("m,n,k,split", [(8, 256, 1024, "1"), (16, 256, 1024, "4"), (48, 256, 1024, "2"),
+                                         (1024, 4864, 256, "1")])
+def test_wait_timeout_is_reported_and_recoverable(m, n, k, split, monkeypatch):
+    """(1024, 4864, 256): 152 output tiles of 128 x 256 select the CTA-pair
+    kernel, whose odd CTAs then forward no "stage landed": the even CTAs'
+    MMA waits run out, both CTAs of every pair wind down and meet at their
+    final cluster barrier."""
     a = inputs.random_bf16(m, k, seed=m)
     b = inputs.random_bf16(n, k, seed=n, std=0.3)
     packed, bq, bs = packed_from_oracle(b)
