@@ -246,11 +246,12 @@ def test_pair_kernel_more_tiles_than_pairs_and_missing_row_tile():
     """m=1100, n=4856, k=800: 5 x 19 = 95 tiles of 256 x 256 on the CTA pairs,
     so some pairs take two tiles and the ring runs across tiles; the last row
     tile pair has rows 1024-1099 in the even CTA and no activation rows at all
-    in the odd one; the last stage holds one and a bit K blocks (K tail 32)."""
+    in the odd one; the last stage holds one and a bit K blocks (K tail 32);
+    C's row stride is 4872 elements."""
     m, n, k = 1100, 4856, 800
     a = inputs.random_bf16(m, k, seed=91)
     b = inputs.random_bf16(n, k, seed=92, std=0.2)
     packed, bq, bs = packed_from_oracle(b)
-    got, c_full = _run(a, packed, ldc=n + 8)
+    got, c_full = _run(a, packed, ldc=n + 16)
     assert_close_to_ref(got, _oracle_full(a, bq, bs), what="pair kernel, 95 tiles")
     assert torch.isnan(c_full[:, n:]).all()
