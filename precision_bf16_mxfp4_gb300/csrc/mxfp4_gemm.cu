@@ -705,12 +705,12 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
 // (multicast).  The epilogue warps read their accumulator rows into
 // registers and arrive on their CTA's acc_empty; in the odd CTA warp 0 then
 // forwards that to the even CTA's acc_empty; their global stores overlap
-// the next tile's MMAs.  Only two kinds of arrival cross between the CTAs,
-// both relaxed (they publish nothing the phases they forward have not
-// already made visible in the odd CTA), and their senders and the MMA thread
-// poll: on GB300 a cluster-scope release arrive stalls the issuing thread
-// while the SM's global stores are in flight, and a suspended try_wait
-// notices a remote arrival late.
+// the next tile's MMAs.  Only two kinds of thread-issued arrival cross
+// between the CTAs, both relaxed (they publish nothing the phases they
+// forward have not already made visible in the odd CTA), and their senders
+// and the MMA thread poll: on GB300 a cluster-scope release arrive stalls the
+// issuing thread while the SM's global stores are in flight, and a suspended
+// try_wait notices a remote arrival late.
 //
 // Warps: 0-7 epilogue (two per 32-lane quadrant, 128 columns each), 8-11
 // scale factors, 12 activation copies (and setup), 13 tensor memory and MMA
