@@ -204,6 +204,22 @@ def test_prepack_b_bf16_equals_quant_then_prepack(n, k, ldb):
     assert torch.equal(one.buf, two.buf)
 
 
+def test_quant_image_into_an_existing_image():
+    """quant_image(a, out=img) overwrites img in place with the same bytes a
+    fresh image gets; an image of another shape is refused."""
+    a1 = inputs.random_bf16(200, 544, seed=5).cuda()
+    a2 = inputs.random_bf16(200, 544, seed=6).cuda()
+    img = mx.quant_image(a1)
+    buf = img.buf
+    again = mx.quant_image(a2, out=img)
+    fresh = mx.quant_image(a2)
+    torch.cuda.synchronize()
+    assert again.buf.data_ptr() == buf.data_ptr()
+    assert torch.equal(again.buf, fresh.buf)
+    with pytest.raises(ValueError):
+        mx.quant_image(inputs.random_bf16(100, 544, seed=7).cuda(), out=img)
+
+
 @pytest.mark.parametrize("m,n,k", [(4, 2880, 512), (32, 520, 2080), (33, 256, 512), (64, 384, 2048),
                                    (200, 256, 2048), (1000, 4856, 544), (2044, 512, 2336)])
 def test_quant_image_then_gemm_image(m, n, k):
