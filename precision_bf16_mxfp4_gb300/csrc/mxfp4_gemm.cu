@@ -696,11 +696,12 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
 // issued, 68 KiB landed - is longer than two stages of MMAs on GB300).  The
 // ring runs continuously across tiles.
 //
-// Hand-offs: each CTA's copies complete on its own full[s], and its scale
-// warps - which write the stage's e8m0 atoms, read straight from the operand
-// images, into their own CTA's tensor memory once the slot's previous MMAs
-// have completed - arrive on its own sf_full[s].  In the odd CTA a relay
-// thread waits for both and makes one arrival on the even CTA's full[s].
+// Hand-offs: a CTA's full[s] completes when its copies have landed and its
+// scale warps - which write the stage's e8m0 atoms, read straight from the
+// operand images, into their own CTA's tensor memory once the slot's
+// previous MMAs have completed - have arrived, so the MMA thread polls one
+// barrier per stage.  In the odd CTA a relay thread waits for that phase and
+// makes one arrival on the even CTA's full[s].
 // The MMA thread's commits arrive on empty[s] and acc_full in both CTAs
 // (multicast).  The epilogue warps read their accumulator rows into
 // registers and arrive on their CTA's acc_empty; in the odd CTA warp 0 then
@@ -730,7 +731,7 @@ struct PairCfg {
   static constexpr int kStgWarpBytes = 32 * kStgPitch * 2;
   static constexpr int kEpiWarps = 8;
   static constexpr int kOffBars = kOffStg + kEpiWarps * kStgWarpBytes;
-  static constexpr int kNumBars = 3 * kStages + 2;  // full, sf_full, empty per stage; acc_full, acc_empty
+  static constexpr int kNumBars = 2 * kStages + 2;  // full, empty per stage; acc_full, acc_empty
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -742,8 +743,10 @@ struct PairCfg {
   static_assert(BN + kStages * kSfColsPerStage <= kTmemCols, "tensor memory");
   static constexpr int kWarpSf0 = 8, kWarpCopyA = 12, kWarpMma = 13, kWarpCopyB = 14;
   // arrivals on the even CTA's barriers
-  static constexpr int kFullArrivals = 3;                      // own A and B copies, the odd CTA's relay
-  static constexpr int kSfArrivals = 4;                        // the CTA's four scale warps
+  // full[s]: the CTA's A and B copies and its four scale warps; in the even
+  // CTA also the odd CTA's relay
+  static constexpr int kFullArrivalsOdd = 2 + 4;
+  static constexpr int kFullArrivals = kFullArrivalsOdd + 1;
   static constexpr int kAccEmptyArrivals = kEpiWarps + 1;      // own epilogue warps, the odd CTA's forward
 };
 
@@ -754,8 +757,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + P::kOffBars);  // operand bytes landed (even: both CTAs')
-  uint64_t* sf_full = full + P::kStages;                                 // the CTA's scales written
-  uint64_t* empty = sf_full + P::kStages;                                // MMAs done with the stage
+  uint64_t* empty = full + P::kStages;                                   // MMAs done with the stage
   uint64_t* acc_full = empty + P::kStages;                               // accumulator complete
   uint64_t* acc_empty = acc_full + 1;                                    // read out (even: by both CTAs)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P::kOffMisc);
@@ -778,8 +780,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
 
   if (threadIdx.x == P::kWarpCopyA * 32) {
     for (int s = 0; s < P::kStages; ++s) {
-      mbar_init(&full[s], rank == 0 ? P::kFullArrivals : 2);
-      mbar_init(&sf_full[s], P::kSfArrivals);
+      mbar_init(&full[s], rank == 0 ? P::kFullArrivals : P::kFullArrivalsOdd);
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
@@ -901,7 +902,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       tmem_store_wait();  // the source registers are reused below
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sf_full[s]);
+      if (lane == 0) mbar_arrive(&full[s]);  // scales in place (the copies arrive with their bytes)
       if (++s == P::kStages) {
         s = 0;
         ph ^= 1;
@@ -924,7 +925,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         bool stop = false;
         for (int64_t tile = pair; tile < total && !stop; tile += pairs) {
           for (int ss = 0; ss < nss; ++ss) {
-            if (!wait_bounded_poll(&full[s], ph, abort_flag) || !wait_bounded_poll(&sf_full[s], ph, abort_flag)) {
+            if (!wait_bounded_poll(&full[s], ph, abort_flag)) {
               stop = true;
               break;
             }
@@ -958,7 +959,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       for (int64_t tile = pair; tile < total && !aborted; tile += pairs, ++it) {
         if (!wait_bounded_poll(acc_empty, (it & 1) ^ 1, abort_flag)) break;  // previous tile read out
         for (int ss = 0; ss < nss; ++ss) {
-          if (!wait_bounded_poll(&full[s], ph, abort_flag) || !wait_bounded_poll(&sf_full[s], ph, abort_flag)) {
+          if (!wait_bounded_poll(&full[s], ph, abort_flag)) {
             aborted = true;
             break;
           }
