@@ -704,14 +704,14 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
 // makes one arrival on the even CTA's full[s].
 // The MMA thread's commits arrive on empty[s] and acc_full in both CTAs
 // (multicast).  The epilogue warps read their accumulator rows into
-// registers and arrive on their CTA's acc_empty; in the odd CTA warp 0 then
-// forwards that to the even CTA's acc_empty; their global stores overlap
-// the next tile's MMAs.  Only two kinds of thread-issued arrival cross
-// between the CTAs, both relaxed (they publish nothing the phases they
-// forward have not already made visible in the odd CTA), and their senders
-// and the MMA thread poll: on GB300 a cluster-scope release arrive stalls the
-// issuing thread while the SM's global stores are in flight, and a suspended
-// try_wait notices a remote arrival late.
+// registers and arrive on the even CTA's acc_empty; their global stores
+// overlap the next tile's MMAs.  Only two kinds of thread-issued arrival
+// cross between the CTAs - the relay's and the odd epilogue warps' - both
+// relaxed (they publish nothing: the bytes and scales they report are in
+// place, the accumulator reads they report have completed), and the threads
+// that wait for them poll: on GB300 a cluster-scope release arrive stalls
+// the issuing thread while the SM's global stores are in flight, and a
+// suspended try_wait notices a remote arrival late.
 //
 // Warps: 0-7 epilogue (two per 32-lane quadrant, 128 columns each), 8-11
 // scale factors, 12 activation copies (and setup), 13 tensor memory and MMA
@@ -747,7 +747,7 @@ struct PairCfg {
   // CTA also the odd CTA's relay
   static constexpr int kFullArrivalsOdd = 2 + 4;
   static constexpr int kFullArrivals = kFullArrivalsOdd + 1;
-  static constexpr int kAccEmptyArrivals = kEpiWarps + 1;      // own epilogue warps, the odd CTA's forward
+  static constexpr int kAccEmptyArrivals = 2 * kEpiWarps;      // the epilogue warps of both CTAs
 };
 
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
@@ -784,7 +784,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, rank == 0 ? P::kAccEmptyArrivals : P::kEpiWarps);
+    mbar_init(acc_empty, P::kAccEmptyArrivals);  // used in the even CTA
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1024,12 +1024,13 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);  // accumulator rows read out: free for the next tile
-      if (rank == 1 && warp == 0 && lane == 0) {
-        // Forward once all eight have arrived.  The reads have completed
-        // (tcgen05.wait::ld), nothing is published: a relaxed arrival, which
-        // does not wait for this thread's stores of the previous tile.
-        if (wait_bounded_poll(acc_empty, it & 1, abort_flag)) mbar_arrive_remote_relaxed(even_bar(acc_empty));
+      // Accumulator rows read out: free for the next tile.  The odd CTA's
+      // warps arrive on the even CTA's barrier directly; their reads have
+      // completed (tcgen05.wait::ld) and nothing is published, so the arrival
+      // is relaxed and does not wait for the warp's stores of the previous tile.
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(acc_empty);
+        else mbar_arrive_remote_relaxed(even_bar(acc_empty));
       }
       if (!ok) continue;
       const int64_t m0 = (tile % tiles_m) * (2 * kTileRows) + rank * kTileRows + quad * 32;
