@@ -965,23 +965,32 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
           }
           tc_fence_after();
           const int cnt = stage_kblocks(ss);
+          const uint64_t off0 = (uint64_t)((s * P::kStageOpBytes) >> 4);
+          const uint32_t sf0 = tmem + P::BN + s * P::kSfColsPerStage;
+          if (cnt == 2 && (int64_t)ss * P::kSuperK + 1 < kt_whole) {  // the usual stage: all eight MMAs in one go
+            constexpr uint64_t kNext = kTileBytes >> 4;
+            mma_mxf4_pair_kblock2(tmem, adesc0 + off0, bdesc0 + off0, adesc0 + off0 + kNext, bdesc0 + off0 + kNext, ie,
+                                  io, sf0, sf0 + 8, sf0 + P::kSfColsPerBlock, sf0 + P::kSfColsPerBlock + 8,
+                                  ss > 0 ? 1u : 0u);
+          } else {
 #pragma unroll
-          for (int j = 0; j < P::kSuperK; ++j) {
-            if (j >= cnt) break;
-            const uint32_t sf = tmem + P::BN + s * P::kSfColsPerStage + j * P::kSfColsPerBlock;
-            const uint32_t acc = (ss > 0 || j > 0) ? 1u : 0u;
-            const int64_t kt = (int64_t)ss * P::kSuperK + j;
-            const uint64_t off = (uint64_t)((s * P::kStageOpBytes + j * kTileBytes) >> 4);
-            const uint64_t ad = adesc0 + off, bd = bdesc0 + off;
-            if (kt < kt_whole) {  // a whole K block: its four MMAs in one go
-              mma_mxf4_pair_kblock(tmem, ad, bd, ie, io, sf, sf + 8, acc);
-            } else {
-              const int steps = k_steps(args.k, kt);
-              for (int kk = 0; kk < steps; ++kk) {
-                // advancing the start address by 32 bytes = 2 in the descriptor's 16-byte units
-                const uint64_t adv = (uint64_t)(kk * 2);
-                mma_mxf4_pair(tmem, ad + adv, bd + adv, (kk & 1) ? io : ie,
-                              sf + (uint32_t)(kk >> 1) * 4, sf + 8 + (uint32_t)(kk >> 1) * 8, (acc || kk > 0) ? 1u : 0u);
+            for (int j = 0; j < P::kSuperK; ++j) {
+              if (j >= cnt) break;
+              const uint32_t sf = tmem + P::BN + s * P::kSfColsPerStage + j * P::kSfColsPerBlock;
+              const uint32_t acc = (ss > 0 || j > 0) ? 1u : 0u;
+              const int64_t kt = (int64_t)ss * P::kSuperK + j;
+              const uint64_t off = (uint64_t)((s * P::kStageOpBytes + j * kTileBytes) >> 4);
+              const uint64_t ad = adesc0 + off, bd = bdesc0 + off;
+              if (kt < kt_whole) {  // a whole K block: its four MMAs in one go
+                mma_mxf4_pair_kblock(tmem, ad, bd, ie, io, sf, sf + 8, acc);
+              } else {
+                const int steps = k_steps(args.k, kt);
+                for (int kk = 0; kk < steps; ++kk) {
+                  // advancing the start address by 32 bytes = 2 in the descriptor's 16-byte units
+                  const uint64_t adv = (uint64_t)(kk * 2);
+                  mma_mxf4_pair(tmem, ad + adv, bd + adv, (kk & 1) ? io : ie,
+                                sf + (uint32_t)(kk >> 1) * 4, sf + 8 + (uint32_t)(kk >> 1) * 8, (acc || kk > 0) ? 1u : 0u);
+                }
               }
             }
           }

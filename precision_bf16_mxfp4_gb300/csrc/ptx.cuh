@@ -208,6 +208,34 @@ __device__ __forceinline__ void mma_mxf4_pair_kblock(uint32_t d, uint64_t a, uin
       ::"r"(d), "l"(a), "l"(b), "r"(idesc_even), "r"(idesc_odd), "r"(sfa), "r"(sfb), "r"(accumulate)
       : "memory");
 }
+// Two consecutive 256-K blocks of a 256 x 256 pair MMA (eight MMAs) from
+// one asm block: the second block's operands at a2 / b2 and its scales at
+// sfa2 / sfb2 (same layout as the first's).
+__device__ __forceinline__ void mma_mxf4_pair_kblock2(uint32_t d, uint64_t a, uint64_t b, uint64_t a2, uint64_t b2,
+                                                      uint32_t idesc_even, uint32_t idesc_odd, uint32_t sfa,
+                                                      uint32_t sfb, uint32_t sfa2, uint32_t sfb2,
+                                                      uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, a3, a5, c1, c3, c5, e1, e3, e5, f1, f3, f5;\n\t"
+      ".reg .b32 sa1, sb1, sa3, sb3;\n\t"
+      "setp.ne.b32 p, %11, 0;\n\tsetp.eq.b32 q, %11, %11;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 a3, %1, 4;\n\tadd.s64 a5, %1, 6;\n\t"
+      "add.s64 c1, %2, 2;\n\tadd.s64 c3, %2, 4;\n\tadd.s64 c5, %2, 6;\n\t"
+      "add.s64 e1, %3, 2;\n\tadd.s64 e3, %3, 4;\n\tadd.s64 e5, %3, 6;\n\t"
+      "add.s64 f1, %4, 2;\n\tadd.s64 f3, %4, 4;\n\tadd.s64 f5, %4, 6;\n\t"
+      "add.u32 sa1, %7, 4;\n\tadd.u32 sb1, %8, 8;\n\tadd.u32 sa3, %9, 4;\n\tadd.u32 sb3, %10, 8;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %5, [%7], [%8], p;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], a1, c1, %6, [%7], [%8], q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], a3, c3, %5, [sa1], [sb1], q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], a5, c5, %6, [sa1], [sb1], q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %3, %4, %5, [%9], [%10], q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], e1, f1, %6, [%9], [%10], q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], e3, f3, %5, [sa3], [sb3], q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], e5, f5, %6, [sa3], [sb3], q;\n\t}"
+      ::"r"(d), "l"(a), "l"(b), "l"(a2), "l"(b2), "r"(idesc_even), "r"(idesc_odd), "r"(sfa), "r"(sfb), "r"(sfa2),
+      "r"(sfb2), "r"(accumulate)
+      : "memory");
+}
 // Arrive once on the mbarrier at `bar`'s offset in each CTA of `cta_mask`
 // when every tcgen05 operation this thread issued before it has completed.
 __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
