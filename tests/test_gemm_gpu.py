@@ -263,6 +263,21 @@ def test_persistent_tile_loop_with_ragged_tails():
     assert torch.isnan(c_full[:, n:]).all()
 
 
+def test_pair_kernel_missing_weight_row_tile():
+    """m=1024, n=4700, k=256: 8 x 19 = 152 tiles of 128 x 256 select the CTA-pair
+    kernel; the last column tile covers weight rows 4608..4863 but the weights
+    end at 4700, so the odd CTA of that tile has no weight row tile at all (it
+    copies nothing and writes zero scales for it) and the even CTA's tile is
+    ragged (92 of 128 rows)."""
+    m, n, k = 1024, 4700, 256
+    a = inputs.random_bf16(m, k, seed=93)
+    b = inputs.random_bf16(n, k, seed=94, std=0.2)
+    packed, bq, bs = packed_from_oracle(b)
+    got, c_full = _run(a, packed, ldc=n + 4)
+    assert_close_to_ref(got, _oracle_full(a, bq, bs), what="pair kernel, missing weight tile")
+    assert torch.isnan(c_full[:, n:]).all()
+
+
 def test_pair_kernel_more_tiles_than_pairs_and_missing_row_tile():
     """m=1100, n=4856, k=800: 5 x 19 = 95 tiles of 256 x 256 on the CTA pairs,
     so some pairs take two tiles and the ring runs across tiles; the last row
