@@ -43,6 +43,8 @@
 // 2-9 quantize the activations and write the scales, and warps 6-9 also drain
 // the accumulator when BN = 32.  Every wait is bounded: a wait that runs out
 // sets a device flag and the CTA winds down.
+#include <cuda.h>  // CUtensorMap (a type only: the library links no driver symbol)
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -725,10 +727,11 @@ struct PairCfg {
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kStages * kStageOpBytes;
   static constexpr int kOffStg = kOffB + kStages * kStageOpBytes;
-  // epilogue staging: per warp, 32 rows x 32 columns of bf16 (+8 pad)
+  // epilogue staging: per warp one box of 32 rows x 32 columns of bf16 (64-byte
+  // rows, 64-byte swizzle: 16-byte chunk q of row r at q ^ ((r >> 1) & 3)),
+  // stored to C by a tensor-map bulk store
   static constexpr int kStgCols = 32;
-  static constexpr int kStgPitch = kStgCols + 8;
-  static constexpr int kStgWarpBytes = 32 * kStgPitch * 2;
+  static constexpr int kStgWarpBytes = 32 * kStgCols * 2;
   static constexpr int kEpiWarps = 8;
   static constexpr int kOffBars = kOffStg + kEpiWarps * kStgWarpBytes;
   static constexpr int kNumBars = 2 * kStages + 2;  // full, empty per stage; acc_full, acc_empty
@@ -751,7 +754,7 @@ struct PairCfg {
 };
 
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
-    gemm_pair_kernel(const GemmArgs args, int64_t tiles_m, int64_t tiles_n) {
+    gemm_pair_kernel(const GemmArgs args, int64_t tiles_m, int64_t tiles_n, const __grid_constant__ CUtensorMap c_map) {
   // tiles_m: 256-row pair tiles of C; tiles_n: 256-column tiles of C
   using P = PairCfg;
   extern __shared__ uint8_t smem_raw[];
@@ -1013,7 +1016,8 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     // stores.
     constexpr int kCols = P::BN / 2;
     const int quad = warp % 4, half = warp / 4;
-    __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem + P::kOffStg + warp * P::kStgWarpBytes);
+    uint8_t* box = smem + P::kOffStg + warp * P::kStgWarpBytes;
+    const int64_t n_tma = args.n & ~int64_t(7);  // the columns the box stores cover
     uint32_t it = 0;
     for (int64_t tile = pair; tile < total; tile += pairs, ++it) {
       const bool ok = wait_bounded_poll(acc_full, it & 1, abort_flag);
@@ -1044,37 +1048,41 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       if (!ok) continue;
       const int64_t m0 = (tile % tiles_m) * (2 * kTileRows) + rank * kTileRows + quad * 32;
       const int64_t n0 = (tile / tiles_m) * P::BN + half * kCols;
-      // 32-column chunks through the warp's staging slice: each lane writes
-      // its row's 64 bytes, then every store instruction covers eight 64-byte
-      // row segments (few, wide transactions for the LSU)
+      // 32-column chunks: each lane writes its row's 64 bytes into the warp's
+      // swizzled box, then one lane stores the box with a tensor-map bulk
+      // store (rows >= m and columns >= n are clipped by the copy engine)
 #pragma unroll
       for (int cc = 0; cc < kCols / P::kStgCols; ++cc) {
-        uint4* row_dst = reinterpret_cast<uint4*>(stg + lane * P::kStgPitch);
+        if (lane == 0) bulk_wait_group_read0();  // the previous store has read the box
+        __syncwarp();
+        uint8_t* row_dst = box + lane * (P::kStgCols * 2);
 #pragma unroll
         for (int q = 0; q < P::kStgCols / 8; ++q) {
           const int c = cc * (P::kStgCols / 16) + (q >> 1), h = q & 1;
-          row_dst[q] = make_uint4(packed[c][4 * h], packed[c][4 * h + 1], packed[c][4 * h + 2], packed[c][4 * h + 3]);
+          *reinterpret_cast<uint4*>(row_dst + ((q ^ ((lane >> 1) & 3)) << 4)) =
+              make_uint4(packed[c][4 * h], packed[c][4 * h + 1], packed[c][4 * h + 2], packed[c][4 * h + 3]);
         }
+        fence_proxy_async_smem();
         __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 32 * P::kStgCols / 256; ++i) {  // 256 columns x rows per instruction
-          constexpr int kLanesPerRow = P::kStgCols / 8;
-          const int row = i * (32 / kLanesPerRow) + lane / kLanesPerRow, ch = lane % kLanesPerRow;
-          const int64_t mi = m0 + row;
-          const int64_t n = n0 + cc * P::kStgCols + ch * 8;
-          if (mi < args.m && n < args.n) {
-            const __nv_bfloat16* src = stg + row * P::kStgPitch + ch * 8;
-            __nv_bfloat16* dst = args.c + mi * args.ldc + n;
-            if (n + 8 <= args.n) {
-              *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-            } else {
-              for (int e = 0; e < 8 && n + e < args.n; ++e) dst[e] = src[e];
-            }
+        const int64_t x0 = n0 + cc * P::kStgCols;
+        if (lane == 0) {
+          tma_store_2d(&c_map, box, (int)x0, (int)m0);
+          bulk_commit_group();
+        }
+        // The tensor map ends at n rounded down to 8 columns (the copy engine
+        // clips whole 16-byte chunks only); the last n mod 8 columns of a row
+        // are stored here, from the same box.
+        if (x0 + P::kStgCols > n_tma && x0 < args.n && m0 + lane < args.m) {
+          for (int64_t col = n_tma > x0 ? n_tma : x0; col < args.n && col < x0 + P::kStgCols; ++col) {
+            const int j = (int)(col - x0);
+            const uint16_t v = *reinterpret_cast<const uint16_t*>(
+                row_dst + ((((j * 2) >> 4) ^ ((lane >> 1) & 3)) << 4) + ((j * 2) & 15));
+            *reinterpret_cast<uint16_t*>(args.c + (m0 + lane) * args.ldc + col) = v;
           }
         }
-        __syncwarp();  // the next chunk reuses the staging slice
       }
     }
+    if (lane == 0) bulk_wait_group0();  // every store of this warp has completed
   }
 
   // Neither CTA frees its tensor memory or exits while the pair still needs
@@ -1135,7 +1143,9 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan, bool a_image
     p.swap_ab = false;
     p.mode = kImagePlain;
     const int64_t mt = ceil_div(m, kTileRows);
-    p.bn = (mt * ceil_div(n, 256) >= sms) ? 256 : 128;
+    // the CTA-pair kernel wants at least one full 256-column tile (its C box
+    // stores need n >= 8) and a tile per SM
+    p.bn = (n >= 256 && mt * ceil_div(n, 256) >= sms) ? 256 : 128;
     p.grid_x = mt;
     const int64_t nt = ceil_div(n, p.bn);
     const int s_max = p.bn == 256 ? 1 : 8;  // the kernels' kMaxSplit
@@ -1265,6 +1275,32 @@ static int max_resident_pairs() {
   return cache[dev];
 }
 
+// The tensor map of C (bf16 [m, n], row stride ldc) for the pair kernel's
+// box stores: boxes of 32 rows x 32 columns, 64-byte swizzle.  The encoder
+// comes from the driver through the runtime's entry-point query.
+static cudaError_t encode_c_map(const GemmArgs& args, CUtensorMap* map) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  // n rounded down to 8 columns: the copy engine clips whole 16-byte chunks,
+  // so a map to n itself would write up to 7 columns past it
+  const cuuint64_t dims[2] = {(cuuint64_t)(args.n & ~int64_t(7)), (cuuint64_t)args.m};
+  const cuuint64_t strides[1] = {(cuuint64_t)args.ldc * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)PairCfg::kStgCols, 32};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, args.c, dims, strides, box, elem_strides,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 static cudaError_t launch_pair(const GemmPlan& plan, const GemmArgs& args, int64_t tiles_m, int64_t tiles_n,
                                cudaStream_t stream) {
   static bool attr_done[64] = {false};
@@ -1293,7 +1329,10 @@ static cudaError_t launch_pair(const GemmPlan& plan, const GemmArgs& args, int64
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel, args, tiles_m, tiles_n);
+  CUtensorMap c_map;
+  const cudaError_t e = encode_c_map(args, &c_map);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel, args, tiles_m, tiles_n, c_map);
 }
 
 cudaError_t launch_gemm(const GemmPlan& plan, const void* a_bf16, int64_t m, int64_t k, int64_t lda,

@@ -374,6 +374,17 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_caddr, const v
       : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Tiled bulk store of a 2-D box from this CTA's shared memory to global
+// memory through a tensor map (a kernel parameter); coordinates (x, y) in
+// elements, x innermost.  Elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const void* tensor_map, const void* src_smem, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tensor_map)),
+               "r"(smem_addr(src_smem)), "r"(x), "r"(y)
+               : "memory");
+}
+// Wait until this thread's committed bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Wait until the source buffers of this thread's committed bulk copies have been read.
 __device__ __forceinline__ void bulk_wait_group_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
