@@ -263,6 +263,20 @@ def test_persistent_tile_loop_with_ragged_tails():
     assert torch.isnan(c_full[:, n:]).all()
 
 
+def test_many_row_tiles_but_narrow_n_avoids_the_pair_kernel():
+    """m=19456, n=200, k=256: 152 row tiles of 128 but not one full 256-column
+    tile, so the planner keeps the one-CTA image kernel (the CTA-pair
+    kernel's C box stores need n >= 8 and it wants full 256-column tiles);
+    the result matches the oracle."""
+    m, n, k = 19456, 200, 256
+    a = inputs.random_bf16(m, k, seed=95)
+    b = inputs.random_bf16(n, k, seed=96, std=0.2)
+    packed, bq, bs = packed_from_oracle(b)
+    got, c_full = _run(a, packed, ldc=n + 8)
+    assert_close_to_ref(got, _oracle_full(a, bq, bs), what="narrow n, many row tiles")
+    assert torch.isnan(c_full[:, n:]).all()
+
+
 def test_pair_kernel_missing_weight_row_tile():
     """m=1024, n=4700, k=256: 8 x 19 = 152 tiles of 128 x 256 select the CTA-pair
     kernel; the last column tile covers weight rows 4608..4863 but the weights
