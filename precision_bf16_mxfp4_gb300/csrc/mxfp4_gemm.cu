@@ -745,12 +745,12 @@ struct PairCfg {
   static constexpr int kTmemCols = 512;
   static_assert(BN + kStages * kSfColsPerStage <= kTmemCols, "tensor memory");
   static constexpr int kWarpSf0 = 8, kWarpCopyA = 12, kWarpMma = 13, kWarpCopyB = 14;
-  // arrivals on the even CTA's barriers
-  // full[s]: the CTA's A and B copies and its four scale warps; in the even
-  // CTA also the odd CTA's relay
+  // barrier arrival counts.  full[s]: the CTA's A and B copies and its four
+  // scale warps, in the even CTA also the odd CTA's relay; acc_empty (used in
+  // the even CTA): the epilogue warps of both CTAs
   static constexpr int kFullArrivalsOdd = 2 + 4;
   static constexpr int kFullArrivals = kFullArrivalsOdd + 1;
-  static constexpr int kAccEmptyArrivals = 2 * kEpiWarps;      // the epilogue warps of both CTAs
+  static constexpr int kAccEmptyArrivals = 2 * kEpiWarps;
 };
 
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
@@ -759,7 +759,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   using P = PairCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P::kOffBars);  // operand bytes landed (even: both CTAs')
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P::kOffBars);  // bytes landed, scales written (even: both CTAs')
   uint64_t* empty = full + P::kStages;                                   // MMAs done with the stage
   uint64_t* acc_full = empty + P::kStages;                               // accumulator complete
   uint64_t* acc_empty = acc_full + 1;                                    // read out (even: by both CTAs)
@@ -809,9 +809,9 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       if (act) pdl_wait();
       const uint8_t* img = act ? args.a_img : args.b_img;
       uint8_t* ring = smem + (act ? P::kOffA : P::kOffB);
-      int64_t g = 0;  // stages issued so far
-      int s = 0;      // its slot
-      uint32_t ph = 0;
+      int64_t g = 0;    // stages issued so far
+      int s = 0;        // slot of stage g
+      uint32_t ph = 0;  // phase parity of that slot's round
       bool stop = false;
       for (int64_t tile = pair; tile < total && !stop; tile += pairs) {
         const int64_t rt = (act ? tile % tiles_m : tile / tiles_m) * 2 + rank;
@@ -1050,7 +1050,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       const int64_t n0 = (tile / tiles_m) * P::BN + half * kCols;
       // 32-column chunks: each lane writes its row's 64 bytes into the warp's
       // swizzled box, then one lane stores the box with a tensor-map bulk
-      // store (rows >= m and columns >= n are clipped by the copy engine)
+      // store (rows >= m and columns past the map's end are not written)
 #pragma unroll
       for (int cc = 0; cc < kCols / P::kStgCols; ++cc) {
         if (lane == 0) bulk_wait_group_read0();  // the previous store has read the box
