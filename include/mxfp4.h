@@ -127,6 +127,32 @@ MXFP4_API mxfp4_status mxfp4_gemm(const void* a_bf16, int64_t m, int64_t k, int6
                         void* c_bf16, int64_t ldc, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * mxfp4_gemm_host -- mxfp4_gemm for an A that lives in host memory and a C
+ * that is wanted there: on `stream`, one 2-D copy of A to the device, the
+ * GEMM of mxfp4_gemm, one 2-D copy of C back.  The pages' entry point takes
+ * its input tuple and returns C (submission 752099, `custom_kernel`); this is
+ * that round trip for a caller whose tensors are in host memory.
+ *   a_host   : bf16 [m, k] in host memory, row stride lda elements
+ *   b_packed : image from mxfp4_prepack_b for (n, k), in device memory
+ *   c_host   : bf16 [m, n] in host memory, row stride ldc elements (written)
+ *   a_dev    : device staging for A, bf16 [m, k] with row stride k
+ *   c_dev    : device staging for C, bf16 [m, n8] with n8 = n rounded up to
+ *              a multiple of 8 (row stride n8)
+ *   workspace: as mxfp4_gemm
+ * With page-locked host buffers the call only enqueues; the copy of C has
+ * landed once `stream` has reached it (synchronize before reading c_host).
+ * With pageable host buffers the runtime stages the copies and the call may
+ * block.  The caller owns every buffer; nothing is allocated.
+ * Preconditions: m, n > 0, k > 0, k % 32 == 0, lda >= k, ldc >= n, host
+ * pointers non-null, a_dev / c_dev / b_packed 16-byte aligned.
+ * Errors: MXFP4_ERR_INVALID_ARG, MXFP4_ERR_WORKSPACE, MXFP4_ERR_UNSUPPORTED,
+ * MXFP4_ERR_CUDA (a copy or a launch failed to enqueue).
+ */
+MXFP4_API mxfp4_status mxfp4_gemm_host(const void* a_host, int64_t m, int64_t k, int64_t lda, const void* b_packed,
+                                       int64_t n, void* c_host, int64_t ldc, void* a_dev, void* c_dev,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * mxfp4_prepack_b_bf16 -- the on-device weight path in one call: bf16 B[n,k]
  * (row stride ldb) straight into the prepacked image, bit-identical to
  * mxfp4_quant followed by mxfp4_prepack_b, with no intermediate buffer.  The

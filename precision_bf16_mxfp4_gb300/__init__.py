@@ -20,6 +20,7 @@ from ._lib import (  # noqa: F401  (raw C-ABI names)
     mxfp4_act_image_bytes,
     mxfp4_device_status,
     mxfp4_gemm,
+    mxfp4_gemm_host,
     mxfp4_gemm_image,
     mxfp4_gemm_noalloc,
     mxfp4_gemm_workspace_bytes,
@@ -191,6 +192,44 @@ def gemm(a, packed: PackedB, out=None, workspace=None):
                     ctypes_void(c.data_ptr()), c.stride(0), ctypes_void(ws_ptr), ws_bytes,
                     _stream_handle(a.device))
     _check(st, "mxfp4_gemm")
+    return c
+
+
+def gemm_host(a_host, packed: PackedB, out=None, a_dev=None, c_dev=None, workspace=None):
+    """C = quant(a_host) . B^T for a host-memory A, into host memory, through
+    mxfp4_gemm_host: A's upload, the GEMM and C's download are enqueued on the
+    current stream of B's device.  `out` (bf16 [m, n], host) is created
+    page-locked when not given; the device staging buffers and the workspace
+    are allocated when not given.  The result is in `out` once the stream has
+    reached the download (synchronize before reading it)."""
+    torch = _torch()
+    if a_host.is_cuda:
+        raise ValueError("a_host must be a host tensor (use gemm for device tensors)")
+    if a_host.dtype != torch.bfloat16 or a_host.dim() != 2 or a_host.stride(1) != 1:
+        raise ValueError("a_host must be a 2-D bf16 tensor with unit column stride")
+    m, k = a_host.shape
+    if k != packed.k:
+        raise ValueError("a_host and packed B disagree on k")
+    n, dev = packed.n, packed.buf.device
+    n8 = (n + 7) // 8 * 8
+    c = out if out is not None else torch.empty((m, n), dtype=torch.bfloat16).pin_memory()
+    if c.is_cuda or c.dtype != torch.bfloat16 or c.dim() != 2 or c.stride(1) != 1 or tuple(c.shape) != (m, n):
+        raise ValueError("out must be a host bf16 [m, n] tensor with unit column stride")
+    if a_dev is None:
+        a_dev = torch.empty((m, k), dtype=torch.bfloat16, device=dev)
+    if c_dev is None:
+        c_dev = torch.empty((m, n8), dtype=torch.bfloat16, device=dev)
+    if a_dev.numel() < m * k or c_dev.numel() < m * n8 or not (a_dev.is_cuda and c_dev.is_cuda):
+        raise ValueError("a_dev needs m*k and c_dev m*round_up(n, 8) bf16 elements on the device")
+    need = mxfp4_gemm_workspace_bytes(m, n, k)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = mxfp4_gemm_host(ctypes_void(a_host.data_ptr()), m, k, a_host.stride(0), ctypes_void(packed.buf.data_ptr()),
+                         n, ctypes_void(c.data_ptr()), c.stride(0), ctypes_void(a_dev.data_ptr()),
+                         ctypes_void(c_dev.data_ptr()), ctypes_void(ws_ptr), ws_bytes, _stream_handle(dev))
+    _check(st, "mxfp4_gemm_host")
     return c
 
 

@@ -80,6 +80,27 @@ mxfp4_status mxfp4_gemm(const void* a_bf16, int64_t m, int64_t k, int64_t lda, c
                                       static_cast<cudaStream_t>(stream)));
 }
 
+mxfp4_status mxfp4_gemm_host(const void* a_host, int64_t m, int64_t k, int64_t lda, const void* b_packed, int64_t n,
+                             void* c_host, int64_t ldc, void* a_dev, void* c_dev, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (m <= 0 || n <= 0 || !valid_k(k) || lda < k || ldc < n) return MXFP4_ERR_INVALID_ARG;
+  if (!a_host || !c_host || !a_dev || !c_dev || !aligned16(a_dev) || !aligned16(c_dev)) return MXFP4_ERR_INVALID_ARG;
+  const int64_t n8 = (n + 7) & ~int64_t(7);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t esz = 2;  // bf16
+  // validate everything the GEMM checks before enqueueing the first copy
+  mxfp4::GemmPlan plan;
+  if (!b_packed || !aligned16(b_packed)) return MXFP4_ERR_INVALID_ARG;
+  if (mxfp4::make_gemm_plan(m, n, k, &plan) != 0) return MXFP4_ERR_UNSUPPORTED;
+  if (plan.workspace > 0 && (!workspace || workspace_bytes < plan.workspace)) return MXFP4_ERR_WORKSPACE;
+  if (plan.workspace > 0 && !aligned16(workspace)) return MXFP4_ERR_INVALID_ARG;
+  if (cudaMemcpy2DAsync(a_dev, k * esz, a_host, lda * esz, k * esz, m, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MXFP4_ERR_CUDA;
+  const mxfp4_status s = mxfp4_gemm(a_dev, m, k, k, b_packed, n, c_dev, n8, workspace, workspace_bytes, stream);
+  if (s != MXFP4_OK) return s;
+  return from_cuda(cudaMemcpy2DAsync(c_host, ldc * esz, c_dev, n8 * esz, n * esz, m, cudaMemcpyDeviceToHost, st));
+}
+
 mxfp4_status mxfp4_prepack_b_bf16(const void* b_bf16, int64_t n, int64_t k, int64_t ldb, void* b_packed,
                                   size_t b_packed_bytes, void* stream) {
   if (n <= 0 || !valid_k(k) || ldb < k || (ldb % 8) != 0) return MXFP4_ERR_INVALID_ARG;

@@ -136,6 +136,30 @@ def test_image_entry_points_reject_bad_arguments_without_a_gpu():
     assert mx.mxfp4_gemm_image(fake, 4, 64, fake, 16, P(0x10008), 16, None) == E     # unaligned C
 
 
+def test_host_entry_point_rejects_bad_arguments_without_a_gpu():
+    fake = P(0x10000)  # never dereferenced: every check runs before the first copy is enqueued
+    E = _lib.MXFP4_ERR_INVALID_ARG
+    args = dict(a=fake, m=4, k=64, lda=64, b=fake, n=16, c=fake, ldc=16, ad=fake, cd=fake, ws=None, wsb=0)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return mx.mxfp4_gemm_host(a["a"], a["m"], a["k"], a["lda"], a["b"], a["n"], a["c"], a["ldc"], a["ad"],
+                                  a["cd"], a["ws"], a["wsb"], None)
+
+    assert call(k=48, lda=48) == E                  # k % 32
+    assert call(m=0) == E                           # m == 0
+    assert call(lda=32) == E                        # lda < k
+    assert call(ldc=12) == E                        # ldc < n
+    assert call(a=None) == E                        # null host A
+    assert call(c=None) == E                        # null host C
+    assert call(ad=P(0x10008)) == E                 # unaligned device staging
+    assert call(b=P(0x10008)) == E                  # unaligned packed B
+    assert call(m=256) == _lib.MXFP4_ERR_WORKSPACE  # the GEMM's workspace is checked before any copy
+    # host rows need no alignment: an odd host stride passes validation (only
+    # the workspace check then stops this fake call)
+    assert call(m=256, lda=67) == _lib.MXFP4_ERR_WORKSPACE
+
+
 def test_product_path_does_not_touch_the_oracle():
     pkg = os.path.join(ROOT, "precision_bf16_mxfp4_gb300")
     for dirpath, _, files in os.walk(pkg):

@@ -117,6 +117,27 @@ def test_gemm_ragged_shapes_with_padded_strides(m, n, k):
     assert torch.isnan(c_full[:, n:]).all(), "wrote outside the [m, n] window"
 
 
+@pytest.mark.parametrize("m,n,k", [(32, 2880, 512), (4, 129, 288), (200, 1003, 544), (1024, 4864, 256)])
+def test_gemm_host_round_trip(m, n, k):
+    # host A with a row stride that is not a multiple of 8 elements, host C
+    # inside a wider NaN-filled buffer: C equals the device call bit for bit
+    # and nothing outside the [m, n] window is written
+    a = inputs.random_bf16(m, k, seed=m + 3 * n + 5 * k)
+    b = inputs.random_bf16(n, k, seed=n + k, std=0.5)
+    packed, bq, bs = packed_from_oracle(b)
+    a_big = torch.zeros((m, k + 5), dtype=torch.bfloat16).pin_memory()
+    a_big[:, :k] = a
+    c_big = torch.full((m, n + 3), float("nan"), dtype=torch.bfloat16).pin_memory()
+    out = mx.gemm_host(a_big[:, :k], packed, out=c_big[:, :n])
+    torch.cuda.synchronize()
+    mx.device_status()
+    want = torch.empty((m, (n + 7) // 8 * 8), dtype=torch.bfloat16, device="cuda")[:, :n]  # ldc % 8 == 0
+    want = mx.gemm(a.cuda(), packed, out=want).cpu()
+    assert torch.equal(out.view(torch.int16), want.view(torch.int16))
+    assert torch.isnan(c_big[:, n:]).all(), "wrote outside the [m, n] window"
+    assert_close_to_ref(out.float().numpy(), _oracle_full(a, bq, bs), what=f"{m}x{n}x{k}")
+
+
 def test_gemm_deterministic_and_reusable_workspace():
     for name in ("m16_n2112_k7168", "m256_n3072_k1536"):
         a, b = inputs.make_inputs(name)
