@@ -139,10 +139,15 @@ MXFP4_API mxfp4_status mxfp4_gemm(const void* a_bf16, int64_t m, int64_t k, int6
  *   c_dev    : device staging for C, bf16 [m, n8] with n8 = n rounded up to
  *              a multiple of 8 (row stride n8)
  *   workspace: as mxfp4_gemm
- * With page-locked host buffers the call only enqueues; the copy of C has
- * landed once `stream` has reached it (synchronize before reading c_host).
- * With pageable host buffers the runtime stages the copies and the call may
- * block.  The caller owns every buffer; nothing is allocated.
+ * With page-locked host buffers the call only enqueues; C is complete in
+ * c_host once `stream` has passed the call (synchronize before reading it).
+ * For m <= 32 with page-locked buffers whose row strides are multiples of 8
+ * elements (16-byte aligned rows), the fused kernel reads A from and writes C
+ * to host memory directly (mapped into the device's address space; over
+ * NVLink-C2C on GB300) and the staging buffers are not touched; otherwise
+ * the two copies go through a_dev and c_dev.  With pageable host buffers the
+ * runtime stages the copies and the call may block.  The caller owns every
+ * buffer; nothing is allocated.
  * Preconditions: m, n > 0, k > 0, k % 32 == 0, lda >= k, ldc >= n, host
  * pointers non-null, a_dev / c_dev / b_packed 16-byte aligned.
  * Errors: MXFP4_ERR_INVALID_ARG, MXFP4_ERR_WORKSPACE, MXFP4_ERR_UNSUPPORTED,

@@ -17,6 +17,18 @@ mxfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MXFP4_OK : MXF
 
 bool valid_k(int64_t k) { return k > 0 && (k % 32) == 0; }
 
+// The address through which kernels reach page-locked host memory (mapped
+// into every device's address space under unified addressing), else nullptr
+// (pageable memory, or a pointer the runtime does not know).
+void* mapped_host(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();  // not sticky: keep it out of the launch checks
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 }  // namespace
 
 extern "C" {
@@ -94,6 +106,15 @@ mxfp4_status mxfp4_gemm_host(const void* a_host, int64_t m, int64_t k, int64_t l
   if (mxfp4::make_gemm_plan(m, n, k, &plan) != 0) return MXFP4_ERR_UNSUPPORTED;
   if (plan.workspace > 0 && (!workspace || workspace_bytes < plan.workspace)) return MXFP4_ERR_WORKSPACE;
   if (plan.workspace > 0 && !aligned16(workspace)) return MXFP4_ERR_INVALID_ARG;
+  if (plan.mode == 0) {
+    // The fused small-m kernel reads A with plain loads and writes C with
+    // plain stores, so with page-locked buffers it works on host memory
+    // directly (NVLink-C2C on GB300): no copy on either side.
+    const void* a_map = mapped_host(a_host);
+    void* c_map = a_map ? mapped_host(c_host) : nullptr;
+    if (a_map && c_map && aligned16(a_map) && aligned16(c_map) && (lda % 8) == 0 && (ldc % 8) == 0)
+      return mxfp4_gemm(a_map, m, k, lda, b_packed, n, c_map, ldc, workspace, workspace_bytes, stream);
+  }
   if (cudaMemcpy2DAsync(a_dev, k * esz, a_host, lda * esz, k * esz, m, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return MXFP4_ERR_CUDA;
   const mxfp4_status s = mxfp4_gemm(a_dev, m, k, k, b_packed, n, c_dev, n8, workspace, workspace_bytes, stream);

@@ -117,25 +117,51 @@ def test_gemm_ragged_shapes_with_padded_strides(m, n, k):
     assert torch.isnan(c_full[:, n:]).all(), "wrote outside the [m, n] window"
 
 
-@pytest.mark.parametrize("m,n,k", [(32, 2880, 512), (4, 129, 288), (200, 1003, 544), (1024, 4864, 256)])
-def test_gemm_host_round_trip(m, n, k):
-    # host A with a row stride that is not a multiple of 8 elements, host C
-    # inside a wider NaN-filled buffer: C equals the device call bit for bit
-    # and nothing outside the [m, n] window is written
+HOST_CASES = [(32, 2880, 512), (4, 129, 288), (17, 136, 1024), (200, 1003, 544), (1024, 4864, 256)]
+
+
+@pytest.mark.parametrize("m,n,k", HOST_CASES)
+@pytest.mark.parametrize("layout", ["aligned", "odd_strides", "pageable"])
+def test_gemm_host_round_trip(m, n, k, layout):
+    # C lands in a wider NaN-filled host buffer, equal bit for bit to the
+    # device call, with nothing outside the [m, n] window written.  Aligned
+    # page-locked rows let the small-m plan work on host memory directly;
+    # row strides that are not multiples of 8 elements, or pageable memory,
+    # take the copies through the device staging buffers.
     a = inputs.random_bf16(m, k, seed=m + 3 * n + 5 * k)
     b = inputs.random_bf16(n, k, seed=n + k, std=0.5)
     packed, bq, bs = packed_from_oracle(b)
-    a_big = torch.zeros((m, k + 5), dtype=torch.bfloat16).pin_memory()
+    n8 = (n + 7) // 8 * 8
+    lda, ldc = (k + 5, n + 3) if layout == "odd_strides" else (k + 8, n8 + 8)
+    pin = (lambda t: t) if layout == "pageable" else (lambda t: t.pin_memory())
+    a_big = pin(torch.zeros((m, lda), dtype=torch.bfloat16))
     a_big[:, :k] = a
-    c_big = torch.full((m, n + 3), float("nan"), dtype=torch.bfloat16).pin_memory()
+    c_big = pin(torch.full((m, ldc), float("nan"), dtype=torch.bfloat16))
     out = mx.gemm_host(a_big[:, :k], packed, out=c_big[:, :n])
     torch.cuda.synchronize()
     mx.device_status()
-    want = torch.empty((m, (n + 7) // 8 * 8), dtype=torch.bfloat16, device="cuda")[:, :n]  # ldc % 8 == 0
+    want = torch.empty((m, n8), dtype=torch.bfloat16, device="cuda")[:, :n]  # ldc % 8 == 0
     want = mx.gemm(a.cuda(), packed, out=want).cpu()
     assert torch.equal(out.view(torch.int16), want.view(torch.int16))
     assert torch.isnan(c_big[:, n:]).all(), "wrote outside the [m, n] window"
     assert_close_to_ref(out.float().numpy(), _oracle_full(a, bq, bs), what=f"{m}x{n}x{k}")
+
+
+def test_gemm_host_reuses_its_buffers_across_calls():
+    # the same host buffers, staging and workspace through several calls in a row
+    m, n, k = 32, 2880, 512
+    a1, a2 = inputs.random_bf16(m, k, seed=1), inputs.random_bf16(m, k, seed=2)
+    packed, _, _ = packed_from_oracle(inputs.random_bf16(n, k, seed=3))
+    a_host = torch.empty((m, k), dtype=torch.bfloat16).pin_memory()
+    c_host = torch.empty((m, n), dtype=torch.bfloat16).pin_memory()
+    a_dev = torch.empty((m, k), dtype=torch.bfloat16, device="cuda")
+    c_dev = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    for a in (a1, a2, a1):
+        a_host.copy_(a)
+        mx.gemm_host(a_host, packed, out=c_host, a_dev=a_dev, c_dev=c_dev)
+        torch.cuda.synchronize()
+        want = mx.gemm(a.cuda(), packed).cpu()
+        assert torch.equal(c_host.view(torch.int16), want.view(torch.int16))
 
 
 def test_gemm_deterministic_and_reusable_workspace():
