@@ -688,7 +688,14 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
 // When the output has at least one 128 x 256 tile per SM, the GEMM runs on
 // CTA pairs (clusters of two): each pair computes 256 x 256 output tiles
 // t = pair, pair + pairs, ... with 256 x 256 x 64 block-scaled MMAs
-// (tcgen05 cta_group::2) that the even CTA issues.  CTA r of a pair holds
+// (tcgen05 cta_group::2) that the even CTA issues.  Tiles are numbered
+// along C's rows first (t -> row tile mt = t / tiles_n, column tile
+// nt = t % tiles_n), so a wave of pairs needs a few activation row tiles and
+// every weight tile: the weights are what the copies can fetch while the
+// activation's quantization is still running, and this order measured 2.4 us
+// faster at m = 4096, n = 7168, k = 2048 than walking the columns first
+// (39.5 vs 41.9 us; the GEMM alone on a ready image is the same either way).
+// CTA r of a pair holds
 // activation row tile 2·mt + r and weight row tile 2·nt + r of every K block
 // in its shared memory, and accumulator rows [128r, 128r + 128) in its tensor
 // memory.  Per SM this halves the weight bytes that each MMA reads from
@@ -755,7 +762,8 @@ struct PairCfg {
 
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     gemm_pair_kernel(const GemmArgs args, int64_t tiles_m, int64_t tiles_n, const __grid_constant__ CUtensorMap c_map) {
-  // tiles_m: 256-row pair tiles of C; tiles_n: 256-column tiles of C
+  // tiles_m: 256-row pair tiles of C; tiles_n: 256-column tiles of C; tile t
+  // is row tile t / tiles_n, column tile t % tiles_n
   using P = PairCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -814,7 +822,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       uint32_t ph = 0;  // phase parity of that slot's round
       bool stop = false;
       for (int64_t tile = pair; tile < total && !stop; tile += pairs) {
-        const int64_t rt = (act ? tile % tiles_m : tile / tiles_m) * 2 + rank;
+        const int64_t rt = (act ? tile / tiles_n : tile % tiles_n) * 2 + rank;
         const bool present = rt < (act ? a_row_tiles : b_row_tiles);  // ragged last tile: nothing to copy
         for (int ss = 0; ss < nss; ++ss, ++g) {
           if (!wait_bounded(&empty[s], ph ^ 1, abort_flag)) {
@@ -865,11 +873,11 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         const int64_t kt = (int64_t)ss * P::kSuperK + j;
         if (kt >= KT) break;
         const uint8_t* src[3];
-        const int64_t art = (tile % tiles_m) * 2 + rank;
+        const int64_t art = (tile / tiles_n) * 2 + rank;
         src[0] = art < a_row_tiles ? args.a_img + image_block(art, kt, KT) + kTileDataBytes : nullptr;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          const int64_t brt = (tile / tiles_m) * 2 + t;
+          const int64_t brt = (tile % tiles_n) * 2 + t;
           src[1 + t] = brt < b_row_tiles ? args.b_img + image_block(brt, kt, KT) + kTileDataBytes : nullptr;
         }
         // a missing row tile (ragged edge) gets zero scales; its rows are never stored
@@ -1046,8 +1054,8 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         else mbar_arrive_remote_relaxed(even_bar(acc_empty));
       }
       if (!ok) continue;
-      const int64_t m0 = (tile % tiles_m) * (2 * kTileRows) + rank * kTileRows + quad * 32;
-      const int64_t n0 = (tile / tiles_m) * P::BN + half * kCols;
+      const int64_t m0 = (tile / tiles_n) * (2 * kTileRows) + rank * kTileRows + quad * 32;
+      const int64_t n0 = (tile % tiles_n) * P::BN + half * kCols;
       // 32-column chunks: each lane writes its row's 64 bytes into the warp's
       // swizzled box, then one lane stores the box with a tensor-map bulk
       // store (rows >= m and columns past the map's end are not written)
