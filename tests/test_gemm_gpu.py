@@ -324,6 +324,24 @@ def test_many_row_tiles_but_narrow_n_avoids_the_pair_kernel():
     assert torch.isnan(c_full[:, n:]).all()
 
 
+@pytest.mark.parametrize("m,n,k", [(3000, 2304, 288), (4000, 1536, 544), (1100, 4856, 800)])
+def test_pair_kernel_later_rounds_and_ragged_edges(m, n, k):
+    # More pair tiles than pairs, so each pair walks tiles of several row
+    # tiles; a ragged K tail (288), a partial last row tile (4000) and a
+    # missing odd row tile (1100).  Full output against the oracle, and equal
+    # bit for bit to the same GEMM on a separately made activation image.
+    a = inputs.random_bf16(m, k, seed=m + 7 * n + k)
+    b = inputs.random_bf16(n, k, seed=n + 3 * k, std=0.5)
+    packed, bq, bs = packed_from_oracle(b)
+    got, c_full = _run(a, packed, ldc=n + 8)
+    assert_close_to_ref(got, _oracle_full(a, bq, bs), what=f"{m}x{n}x{k}")
+    assert torch.isnan(c_full[:, n:]).all(), "wrote outside the [m, n] window"
+    img = mx.quant_image(a.cuda())
+    want = mx.gemm_image(img, packed)
+    torch.cuda.synchronize()
+    assert torch.equal(c_full[:, :n].view(torch.int16), want.view(torch.int16))
+
+
 def test_pair_kernel_missing_weight_row_tile():
     """m=1024, n=4700, k=256: 8 x 19 = 152 tiles of 128 x 256 select the CTA-pair
     kernel; the last column tile covers weight rows 4608..4863 but the weights
