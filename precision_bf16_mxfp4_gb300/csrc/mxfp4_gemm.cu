@@ -48,6 +48,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdlib>
 
 #include "mxfp4_device.cuh"
@@ -1105,16 +1106,20 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host
+// The host-side caches below are per device and idempotent (two threads that
+// miss at once compute or set the same value), so relaxed atomics suffice to
+// keep concurrent callers race-free.
 int num_sms() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int v = 0;
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = v > 0 ? v : 148;
+    if (v <= 0) v = 148;
+    cached[dev].store(v, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return v;
 }
 
 // MXFP4_SPLIT_K=<1|2|4|8> overrides the K-split factor the planner picks
@@ -1180,12 +1185,14 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan, bool a_image
 template <int BN, int kMode>
 static int max_resident_clusters(int split) {
   using C = Cfg<BN, kMode>;
-  static int cache[64][4] = {};  // [device][log2 split - 1]
+  static std::atomic<int> cache[64][4];  // [device][log2 split - 1]
   int dev = 0;
   cudaGetDevice(&dev);
   const int idx = split == 2 ? 0 : split == 4 ? 1 : split == 8 ? 2 : 3;
   if (dev < 0 || dev >= 64) return 0;
-  if (cache[dev][idx] == 0) {
+  const int hit = cache[dev][idx].load(std::memory_order_relaxed);
+  if (hit != 0) return hit;
+  {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(1, (unsigned)split, 1);
     cfg.blockDim = dim3(C::kThreads, 1, 1);
@@ -1202,23 +1209,23 @@ static int max_resident_clusters(int split) {
       cudaGetLastError();  // clear the error: the launch decides
       n = -1;
     }
-    cache[dev][idx] = n;
+    cache[dev][idx].store(n, std::memory_order_relaxed);
+    return n;
   }
-  return cache[dev][idx];
 }
 
 template <int BN, int kMode>
 static cudaError_t launch_one(const GemmPlan& plan_in, const GemmArgs& args_in, cudaStream_t stream) {
   using C = Cfg<BN, kMode>;
   if (plan_in.split > C::kMaxSplit) return cudaErrorInvalidConfiguration;
-  static bool attr_done[64] = {false};
+  static std::atomic<bool> attr_done[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_done[dev].load(std::memory_order_relaxed)) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_relaxed);
   }
   // A K split whose clusters cannot all be resident at once would run in two
   // waves; halve it until they fit (the result does not depend on the split).
@@ -1257,11 +1264,13 @@ static cudaError_t launch_one(const GemmPlan& plan_in, const GemmArgs& args_in, 
 
 // CTA pairs of the pair kernel that can be resident at once (cached per device).
 static int max_resident_pairs() {
-  static int cache[64] = {};
+  static std::atomic<int> cache[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return 0;
-  if (cache[dev] == 0) {
+  const int hit = cache[dev].load(std::memory_order_relaxed);
+  if (hit != 0) return hit;
+  {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(PairCfg::kThreads, 1, 1);
@@ -1278,16 +1287,17 @@ static int max_resident_pairs() {
       cudaGetLastError();  // clear the error: the launch decides
       n = -1;
     }
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
+    return n;
   }
-  return cache[dev];
 }
 
 // The tensor map of C (bf16 [m, n], row stride ldc) for the pair kernel's
 // box stores: boxes of 32 rows x 32 columns, 64-byte swizzle.  The encoder
 // comes from the driver through the runtime's entry-point query.
 static cudaError_t encode_c_map(const GemmArgs& args, CUtensorMap* map) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> cached{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 encode = cached.load(std::memory_order_relaxed);
   if (!encode) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q{};
@@ -1296,6 +1306,7 @@ static cudaError_t encode_c_map(const GemmArgs& args, CUtensorMap* map) {
         q != cudaDriverEntryPointSuccess || !fn)
       return cudaErrorNotSupported;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    cached.store(encode, std::memory_order_relaxed);
   }
   // n rounded down to 8 columns: the copy engine clips whole 16-byte chunks,
   // so a map to n itself would write up to 7 columns past it
@@ -1311,14 +1322,14 @@ static cudaError_t encode_c_map(const GemmArgs& args, CUtensorMap* map) {
 
 static cudaError_t launch_pair(const GemmPlan& plan, const GemmArgs& args, int64_t tiles_m, int64_t tiles_n,
                                cudaStream_t stream) {
-  static bool attr_done[64] = {false};
+  static std::atomic<bool> attr_done[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_done[dev].load(std::memory_order_relaxed)) {
     cudaError_t e =
         cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_relaxed);
   }
   int64_t pairs = plan.grid_x / 2;
   const int resident = max_resident_pairs();

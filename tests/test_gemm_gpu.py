@@ -187,6 +187,41 @@ def test_gemm_on_a_side_stream_matches():
     assert_close_to_ref(c.float().cpu().numpy(), _oracle_full(a, bq, bs))
 
 
+def test_gemm_from_several_host_threads():
+    # the entry points are reentrant: four host threads, each on its own
+    # stream, run the fused, split, image and CTA-pair plans at once and get
+    # what a single thread gets
+    import threading
+    shapes = [(32, 2880, 512), (16, 2112, 7168), (256, 3072, 1536), (1024, 4864, 256)]
+    cases = []
+    for i, (m, n, k) in enumerate(shapes):
+        a = inputs.random_bf16(m, k, seed=100 + i).cuda()
+        packed, _, _ = packed_from_oracle(inputs.random_bf16(n, k, seed=200 + i, std=0.5))
+        cases.append((a, packed, mx.gemm(a, packed)))
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(a, packed, want):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(5):
+                    got = mx.gemm(a, packed)
+                    s.synchronize()
+                    if not torch.equal(got.view(torch.int16), want.view(torch.int16)):
+                        errors.append("mismatch")
+        except Exception as e:  # surfaced below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=c) for c in cases]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    mx.device_status()
+
+
 def test_gemm_reports_small_workspace():
     a = inputs.random_bf16(256, 512, seed=1).cuda()
     b = inputs.random_bf16(128, 512, seed=2)
