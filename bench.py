@@ -380,6 +380,23 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
+def measure_fp4_peak(local_rank, kblocks_per_sm=4000, runs=5):
+    """The dense FP4 tensor-core rate (the large-m GEMM's roofline
+    denominator, which the measured-peaks file does not provide): the
+    median of `runs` launches of the library's microbenchmark, with the SM
+    clocks sampled meanwhile."""
+    import torch
+
+    import precision_bf16_mxfp4_gb300 as mx
+    torch.cuda.set_device(local_rank)
+    mx.measure_fp4_peak(200)  # warm-up: module load, attributes
+    with ClockSampler(local_rank) as clk:
+        vals = [mx.measure_fp4_peak(kblocks_per_sm) for _ in range(runs)]
+    return {"fp4_peak_tflops": round(statistics.median(vals), 1), "runs_tflops": [round(v, 1) for v in vals],
+            "kblocks_per_sm": kblocks_per_sm, "sms": torch.cuda.get_device_properties(local_rank).multi_processor_count,
+            "nominal_tflops": NOMINAL_FP4_TFLOPS, "clocks": clk.summary()}
+
+
 def main(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -389,6 +406,8 @@ def main(argv=None):
     p.add_argument("--workload", default="m32_n4096_k512,m32_n2880_k512")
     p.add_argument("--table", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--fp4-peak", action="store_true",
+                   help="measure the dense FP4 tensor-core rate (mxfp4_measure_fp4_peak) and exit")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -402,6 +421,11 @@ def main(argv=None):
         if rank != 0:
             return 0
         print(json.dumps(run_reference(args, names)))
+        return 0
+
+    if args.fp4_peak:
+        if rank == 0:
+            print(json.dumps(measure_fp4_peak(local_rank)))
         return 0
 
     if world > 1:

@@ -235,6 +235,22 @@ MXFP4_API mxfp4_status mxfp4_gemm_noalloc(const void* a_bf16, int64_t m, int64_t
                                           void* stream);
 
 /*
+ * mxfp4_measure_fp4_peak -- the dense block-scaled FP4 tensor-core rate of
+ * the current device, in TFLOP/s, for roofline fractions: one CTA per SM
+ * issues kblocks_per_sm back-to-back 128 x 256 x 256 K blocks of
+ * tcgen05.mma kind::mxf4 (the GEMM kernels' issue sequence) on operands held
+ * in shared memory, and the launch is timed with CUDA events on `stream`.
+ * The pages quote no FP4 peak for this hardware; NVIDIA's nominal dense
+ * figure for GB300 is 13.5 PFLOP/s.
+ *   kblocks_per_sm: 1 .. 2^24 (about 2000 gives a launch of ~1 ms)
+ *   tflops        : out, FLOPs (2 * 128 * 256 * 256 per K block and SM) / time
+ * Blocks the host until the launch has finished (a measurement, not a
+ * pipeline step).  Errors: MXFP4_ERR_INVALID_ARG, MXFP4_ERR_CUDA,
+ * MXFP4_ERR_TIMEOUT (the bounded completion wait ran out).
+ */
+MXFP4_API mxfp4_status mxfp4_measure_fp4_peak(int64_t kblocks_per_sm, double* tflops, void* stream);
+
+/*
  * mxfp4_device_status -- synchronize `stream`, then report and clear the
  * device-side watchdog flag: MXFP4_ERR_TIMEOUT if any kernel of this
  * library on the current device gave up a bounded pipeline wait since the

@@ -24,6 +24,7 @@ from ._lib import (  # noqa: F401  (raw C-ABI names)
     mxfp4_gemm_image,
     mxfp4_gemm_noalloc,
     mxfp4_gemm_workspace_bytes,
+    mxfp4_measure_fp4_peak,
     mxfp4_prepack_b,
     mxfp4_prepack_b_bf16,
     mxfp4_prepacked_b_bytes,
@@ -231,6 +232,18 @@ def gemm_host(a_host, packed: PackedB, out=None, a_dev=None, c_dev=None, workspa
                          ctypes_void(c_dev.data_ptr()), ctypes_void(ws_ptr), ws_bytes, _stream_handle(dev))
     _check(st, "mxfp4_gemm_host")
     return c
+
+
+def measure_fp4_peak(kblocks_per_sm: int = 2000, device=None) -> float:
+    """Dense block-scaled FP4 tensor-core rate of the device in TFLOP/s,
+    measured by mxfp4_measure_fp4_peak (blocks until it has run)."""
+    import ctypes
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    out = ctypes.c_double(0.0)
+    _check(mxfp4_measure_fp4_peak(int(kblocks_per_sm), ctypes.byref(out), _stream_handle(dev)),
+           "mxfp4_measure_fp4_peak")
+    return out.value
 
 
 def gemm_noalloc(a, packed: PackedB, out=None):

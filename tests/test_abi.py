@@ -160,6 +160,15 @@ def test_host_entry_point_rejects_bad_arguments_without_a_gpu():
     assert call(m=256, lda=67) == _lib.MXFP4_ERR_WORKSPACE
 
 
+def test_fp4_peak_rejects_bad_arguments_without_a_gpu():
+    import ctypes
+    out = ctypes.c_double(0.0)
+    E = _lib.MXFP4_ERR_INVALID_ARG
+    assert mx.mxfp4_measure_fp4_peak(0, ctypes.byref(out), None) == E
+    assert mx.mxfp4_measure_fp4_peak(1 << 25, ctypes.byref(out), None) == E
+    assert mx.mxfp4_measure_fp4_peak(100, None, None) == E
+
+
 def test_product_path_does_not_touch_the_oracle():
     pkg = os.path.join(ROOT, "precision_bf16_mxfp4_gb300")
     for dirpath, _, files in os.walk(pkg):

@@ -222,6 +222,15 @@ def test_gemm_from_several_host_threads():
     mx.device_status()
 
 
+def test_fp4_peak_microbenchmark_is_plausible():
+    # a dense FP4 rate between a tenth of NVIDIA's nominal 13.5 PFLOP/s and
+    # a little above it, and roughly proportional to the work asked for
+    small, big = mx.measure_fp4_peak(500), mx.measure_fp4_peak(4000)
+    assert 1350.0 < big < 15000.0, big
+    assert small < big * 1.2
+    mx.device_status()
+
+
 def test_gemm_reports_small_workspace():
     a = inputs.random_bf16(256, 512, seed=1).cuda()
     b = inputs.random_bf16(128, 512, seed=2)
