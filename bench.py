@@ -32,6 +32,7 @@ if ROOT not in sys.path:
 
 METRIC = "MXFP4 GEMM µs + effective TB/s per shape (L2-cold); % of HBM/FP4 roofline"
 NOMINAL_FP4_TFLOPS = 13500.0  # dense FP4 tensor rate, nominal (no measured FP4 peak is available)
+NOMINAL_BF16_TFLOPS = 2250.0  # dense bf16 tensor rate, nominal (for the FP4/bf16 ratio)
 
 
 def algorithmic_bytes(m, n, k):
@@ -221,14 +222,7 @@ def run_ours(args, names, rank, world, local_rank):
                            "tbps": round(byt / med / 1e12, 4), "tflops": round(fl / med / 1e12, 3),
                            "roofline_frac": round(floor_s / med, 4)})
 
-    # dominant kernel: the fused m=32 GEMM launch (one per shape per step)
-    kernel_s = step_s / len(shapes)
-    kernel_bytes = step_bytes / len(shapes)
-    achieved = kernel_bytes / kernel_s / 1e9
-    roofline = {"bound": "hbm", "kernel": "gemm_kernel<32, fused>", "achieved": round(achieved, 2),
-                "peak": hbm_gbs, "unit": "GB/s", "frac": round(achieved / hbm_gbs, 4),
-                "peak_source": f"{peak_src} hbm_gbs", "traffic": profiled_traffic("gemm_fused_bn32"),
-                "algorithmic_bytes_per_launch": int(kernel_bytes)}
+    roofline = dominant_roofline([s["w"] for s in shapes], dev_times, props.multi_processor_count)
 
     out = {
         "metric": METRIC, "value": round(world * step_bytes / step_s_max / 1e12, 5), "unit": "TB/s",
@@ -244,7 +238,7 @@ def run_ours(args, names, rank, world, local_rank):
                 "us_per_step": round(e2e_s * 1e6, 3),
                 "h2d_bytes_per_step": int(sum(s["a_host"].numel() * 2 for s in shapes)),
                 "d2h_bytes_per_step": int(sum(s["c_host"].numel() * 2 for s in shapes))},
-        "gpu_launches": args.steps * len(shapes),
+        "gpu_launches": args.steps * sum(launches_per_gemm(s["w"].m) for s in shapes),
         "roofline": roofline,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 4),
@@ -252,6 +246,66 @@ def run_ours(args, names, rank, world, local_rank):
     if args.table and rank == 0:
         print_table(dev, flush, mx, inputs, hbm_gbs)
     return out
+
+
+def launches_per_gemm(m):
+    """Kernels one mxfp4_gemm call launches: the fused GEMM alone for m <= 32,
+    else the activation quantizer and the GEMM."""
+    return 1 if m <= 32 else 2
+
+
+def gemm_kernel_name(m, n, sms):
+    """The GEMM kernel the library's planner picks for (m, n) (its rule,
+    restated for labelling the roofline)."""
+    if m <= 32:
+        return "gemm_kernel<%d, fused>" % (16 if m <= 16 else 32)
+    if m <= 128:
+        return "gemm_kernel<%d, image swap>" % (64 if m <= 64 else 128)
+    if n >= 256 and -(-m // 128) * -(-n // 256) >= sms:
+        return "gemm_pair_kernel"
+    return "gemm_kernel<128, image plain>"
+
+
+def dominant_roofline(works, dev_times, sms):
+    """Roofline of the step's dominant GEMM (the shape with the most FLOPs),
+    bound by whichever floor is longer at the measured peaks.  HBM-bound
+    (the m <= 32 headline, and m = 4096 with k = 2048): algorithmic bytes per
+    launch over the mean event time per launch against the measured copy
+    bandwidth.  A shape whose FP4 work
+    outweighs its bytes at the peaks (a long-K large-m GEMM; m = 4096 with
+    k = 2048 is still bound by its 56 MiB of C): algorithmic FLOPs over the
+    mean event time of its step, which also covers the activation quantizer
+    that precedes the GEMM (a lower bound for the GEMM alone), against the
+    measured bf16 peak times NVIDIA's nominal FP4/bf16 ratio (13.5 / 2.25)."""
+    hbm_gbs, bf16_tflops, peak_src = load_peaks()
+    fp4_peak = bf16_tflops * (NOMINAL_FP4_TFLOPS / NOMINAL_BF16_TFLOPS)
+    i = max(range(len(works)), key=lambda j: flops(works[j].m, works[j].n, works[j].k))
+    w = works[i]
+    fl, byt = flops(w.m, w.n, w.k), algorithmic_bytes(w.m, w.n, w.k)
+    kernel = gemm_kernel_name(w.m, w.n, sms)
+    if fl / (fp4_peak * 1e12) > byt / (hbm_gbs * 1e9):
+        t = statistics.mean(dev_times[i])
+        achieved = fl / t / 1e12
+        return {"bound": "tensor", "kernel": kernel, "achieved": round(achieved, 1), "peak": round(fp4_peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4),
+                "peak_source": f"{peak_src} bf16_tflops x nominal FP4/bf16 ratio 6",
+                "traffic": profiled_traffic("gemm_pair_m4096") if (w.m, w.n, w.k) == (4096, 7168, 2048) else None,
+                "algorithmic_flops_per_launch": int(fl),
+                "timed": "event pair around quantizer + GEMM (one step of this shape)"}
+    # bandwidth-bound: bytes per launch over the mean time per launch, all shapes
+    kernel_s = sum(statistics.mean(t) for t in dev_times) / len(works)
+    kernel_bytes = sum(algorithmic_bytes(x.m, x.n, x.k) for x in works) / len(works)
+    achieved = kernel_bytes / kernel_s / 1e9
+    if all(16 < x.m <= 32 for x in works):
+        traffic = profiled_traffic("gemm_fused_bn32")
+    elif [(x.m, x.n, x.k) for x in works] == [(4096, 7168, 2048)]:
+        traffic = profiled_traffic("gemm_pair_m4096")
+    else:
+        traffic = None
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 2),
+            "peak": hbm_gbs, "unit": "GB/s", "frac": round(achieved / hbm_gbs, 4),
+            "peak_source": f"{peak_src} hbm_gbs", "traffic": traffic,
+            "algorithmic_bytes_per_launch": int(kernel_bytes)}
 
 
 def print_table(dev, flush, mx, inputs, hbm_gbs, table_iters=200):

@@ -96,3 +96,42 @@ def test_clock_summary_flags_throttle_reasons():
 
 def test_traffic_is_reported_only_for_the_profiled_sources():
     assert bench.profiled_traffic("no_such_kernel") is None
+
+
+class _W:
+    def __init__(self, m, n, k):
+        self.m, self.n, self.k = m, n, k
+
+
+def test_roofline_of_the_headline_is_hbm_bound():
+    works = [_W(32, 4096, 512), _W(32, 2880, 512)]
+    r = bench.dominant_roofline(works, [[9e-6, 9e-6], [9e-6, 9e-6]], 152)
+    hbm, _, _ = bench.load_peaks()
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["kernel"] == "gemm_kernel<32, fused>"
+    per_launch = (bench.algorithmic_bytes(32, 4096, 512) + bench.algorithmic_bytes(32, 2880, 512)) / 2
+    assert r["algorithmic_bytes_per_launch"] == int(per_launch)
+    assert abs(r["achieved"] - per_launch / 9e-6 / 1e9) < 0.01
+    assert abs(r["frac"] - r["achieved"] / hbm) < 1e-4
+
+
+def test_roofline_of_the_large_gemm_picks_the_longer_floor():
+    hbm, bf16, _ = bench.load_peaks()
+    # m = 4096, k = 2048: 83 MB of algorithmic bytes outlast 120 GFLOP at
+    # the peaks (the C write dominates), so the bound is HBM
+    r = bench.dominant_roofline([_W(4096, 7168, 2048)], [[40e-6, 40e-6]], 152)
+    assert r["bound"] == "hbm" and r["kernel"] == "gemm_pair_kernel"
+    assert abs(r["achieved"] - bench.algorithmic_bytes(4096, 7168, 2048) / 40e-6 / 1e9) < 0.01
+    # a long K makes the FP4 work the longer floor: the measured bf16 peak
+    # times the nominal FP4 / bf16 ratio (13.5 / 2.25)
+    r = bench.dominant_roofline([_W(4096, 7168, 16384)], [[100e-6, 100e-6]], 152)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["kernel"] == "gemm_pair_kernel"
+    assert abs(r["peak"] - bf16 * 6) < 0.1
+    assert abs(r["achieved"] - 2 * 4096 * 7168 * 16384 / 100e-6 / 1e12) < 0.1
+
+
+@pytest.mark.parametrize("m,n,name", [(4, 2880, "gemm_kernel<16, fused>"), (32, 4096, "gemm_kernel<32, fused>"),
+                                      (64, 7168, "gemm_kernel<64, image swap>"),
+                                      (256, 3072, "gemm_kernel<128, image plain>"), (4096, 7168, "gemm_pair_kernel")])
+def test_kernel_labels_follow_the_planner(m, n, name):
+    assert bench.gemm_kernel_name(m, n, 152) == name
+    assert bench.launches_per_gemm(m) == (1 if m <= 32 else 2)
