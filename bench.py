@@ -451,6 +451,35 @@ def measure_fp4_peak(local_rank, kblocks_per_sm=4000, runs=5):
             "nominal_tflops": NOMINAL_FP4_TFLOPS, "clocks": clk.summary()}
 
 
+def measure_launch_floor(local_rank, steps, warmup, ctas=32):
+    """The launch floor of the small-m GEMMs: CUDA events around one empty
+    kernel, and around two back to back, each after the same L2 flush the
+    GEMMs get (mean and median over `steps`, in microseconds)."""
+    import torch
+
+    import precision_bf16_mxfp4_gb300 as mx
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    out = {"ctas": ctas, "steps": steps, "l2": "flushed before every timed launch (write of %d MiB)" %
+           (flush.numel() >> 20)}
+    for count in (1, 2):
+        times = []
+        for it in range(warmup + steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            mx.launch_empty(count, ctas)
+            e1.record()
+            torch.cuda.synchronize()
+            if it >= warmup:
+                times.append(e0.elapsed_time(e1) * 1e3)
+        out[f"{count}_kernel_us"] = {"mean": round(statistics.mean(times), 3), "median": round(statistics.median(times), 3)}
+    return out
+
+
 def main(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -462,6 +491,8 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--fp4-peak", action="store_true",
                    help="measure the dense FP4 tensor-core rate (mxfp4_measure_fp4_peak) and exit")
+    p.add_argument("--launch-floor", action="store_true",
+                   help="time one and two empty kernels with the GEMMs' flush + event method and exit")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -480,6 +511,11 @@ def main(argv=None):
     if args.fp4_peak:
         if rank == 0:
             print(json.dumps(measure_fp4_peak(local_rank)))
+        return 0
+
+    if args.launch_floor:
+        if rank == 0:
+            print(json.dumps(measure_launch_floor(local_rank, args.steps, args.warmup)))
         return 0
 
     if world > 1:

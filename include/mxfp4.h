@@ -251,6 +251,14 @@ MXFP4_API mxfp4_status mxfp4_gemm_noalloc(const void* a_bf16, int64_t m, int64_t
 MXFP4_API mxfp4_status mxfp4_measure_fp4_peak(int64_t kblocks_per_sm, double* tflops, void* stream);
 
 /*
+ * mxfp4_launch_empty -- enqueue `count` (1..16) empty kernels of `ctas`
+ * (1..65535) 32-thread CTAs on `stream`: the launch floor the small-m GEMM
+ * (one launch, latency-bound) is measured against with the same event
+ * method.  Errors: MXFP4_ERR_INVALID_ARG, MXFP4_ERR_CUDA.
+ */
+MXFP4_API mxfp4_status mxfp4_launch_empty(int count, int ctas, void* stream);
+
+/*
  * mxfp4_device_status -- synchronize `stream`, then report and clear the
  * device-side watchdog flag: MXFP4_ERR_TIMEOUT if any kernel of this
  * library on the current device gave up a bounded pipeline wait since the

@@ -24,6 +24,7 @@ from ._lib import (  # noqa: F401  (raw C-ABI names)
     mxfp4_gemm_image,
     mxfp4_gemm_noalloc,
     mxfp4_gemm_workspace_bytes,
+    mxfp4_launch_empty,
     mxfp4_measure_fp4_peak,
     mxfp4_prepack_b,
     mxfp4_prepack_b_bf16,
@@ -244,6 +245,13 @@ def measure_fp4_peak(kblocks_per_sm: int = 2000, device=None) -> float:
     _check(mxfp4_measure_fp4_peak(int(kblocks_per_sm), ctypes.byref(out), _stream_handle(dev)),
            "mxfp4_measure_fp4_peak")
     return out.value
+
+
+def launch_empty(count: int = 1, ctas: int = 32, device=None):
+    """Enqueue `count` empty kernels on the current stream (the launch floor)."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _check(mxfp4_launch_empty(int(count), int(ctas), _stream_handle(dev)), "mxfp4_launch_empty")
 
 
 def gemm_noalloc(a, packed: PackedB, out=None):

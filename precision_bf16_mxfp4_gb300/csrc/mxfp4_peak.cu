@@ -5,7 +5,8 @@
 // block-scaled K blocks (tcgen05.mma kind::mxf4, eight MMAs of 128 x 128 x 64
 // per block, the GEMM kernels' own issue sequence) on operands that stay in
 // shared memory; nothing is loaded from or stored to global memory.  The
-// host times the launch with CUDA events and divides the FLOPs by it.
+// host times the launch with CUDA events and divides the FLOPs by it.  Also
+// the launch floor: empty kernels timed the way the GEMMs are.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -94,8 +95,20 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int64_t kbloc
   }
 }
 
+// An empty kernel: the launch floor that the small-m GEMM's time is read against.
+__global__ void empty_kernel() {}
+
 }  // namespace
 }  // namespace mxfp4
+
+extern "C" mxfp4_status mxfp4_launch_empty(int count, int ctas, void* stream) {
+  if (count < 1 || count > 16 || ctas < 1 || ctas > 65535) return MXFP4_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) {
+    mxfp4::empty_kernel<<<ctas, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+    if (cudaGetLastError() != cudaSuccess) return MXFP4_ERR_CUDA;
+  }
+  return MXFP4_OK;
+}
 
 extern "C" mxfp4_status mxfp4_measure_fp4_peak(int64_t kblocks_per_sm, double* tflops, void* stream) {
   using namespace mxfp4;

@@ -169,6 +169,13 @@ def test_fp4_peak_rejects_bad_arguments_without_a_gpu():
     assert mx.mxfp4_measure_fp4_peak(100, None, None) == E
 
 
+def test_launch_empty_rejects_bad_arguments_without_a_gpu():
+    E = _lib.MXFP4_ERR_INVALID_ARG
+    assert mx.mxfp4_launch_empty(0, 32, None) == E
+    assert mx.mxfp4_launch_empty(17, 32, None) == E
+    assert mx.mxfp4_launch_empty(1, 0, None) == E
+
+
 def test_product_path_does_not_touch_the_oracle():
     pkg = os.path.join(ROOT, "precision_bf16_mxfp4_gb300")
     for dirpath, _, files in os.walk(pkg):

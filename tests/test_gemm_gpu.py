@@ -231,6 +231,12 @@ def test_fp4_peak_microbenchmark_is_plausible():
     mx.device_status()
 
 
+def test_launch_floor_kernels_run():
+    mx.launch_empty(2, 32)
+    torch.cuda.synchronize()
+    mx.device_status()
+
+
 def test_gemm_reports_small_workspace():
     a = inputs.random_bf16(256, 512, seed=1).cuda()
     b = inputs.random_bf16(128, 512, seed=2)
