@@ -16,9 +16,11 @@
  *
  * Conventions for every entry point
  *   - Pointers named *_bf16 / a_fp4 / a_scale / b_* / c_* / workspace are
- *     DEVICE pointers of the current CUDA device; the caller allocates and
- *     owns them.  The library never allocates, never synchronizes (except
- *     mxfp4_device_status) and only enqueues work on `stream`.
+ *     DEVICE pointers of the current CUDA device, except a_host / c_host of
+ *     mxfp4_gemm_host; the caller allocates and owns them.  The library
+ *     never allocates, never synchronizes (except mxfp4_device_status and
+ *     the mxfp4_measure_fp4_peak measurement) and only enqueues work on
+ *     `stream`.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
  *   - Element strides (lda, ldc) are in elements, row-major.
  *   - Errors: MXFP4_ERR_INVALID_ARG / MXFP4_ERR_UNSUPPORTED are returned
