@@ -67,6 +67,7 @@ def test_reference_arm_json_line(monkeypatch):
     assert line["impl"] == "reference" and line["unit"] == "TB/s" and line["value"] > 0
     assert line["metric"] == bench.METRIC and line["higher_is_better"] is True
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["host_cores"] >= 1 and line["cpu_baseline"]["cpu_model"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
 
 
@@ -99,34 +100,70 @@ def test_traffic_is_reported_only_for_the_profiled_sources():
 
 
 class _W:
-    def __init__(self, m, n, k):
-        self.m, self.n, self.k = m, n, k
+    def __init__(self, m, n, k, name="w"):
+        self.m, self.n, self.k, self.name = m, n, k, name
 
 
-def test_roofline_of_the_headline_is_hbm_bound():
-    works = [_W(32, 4096, 512), _W(32, 2880, 512)]
-    r = bench.dominant_roofline(works, [[9e-6, 9e-6], [9e-6, 9e-6]], 152)
+def test_fp4_peak_is_the_measured_bf16_rate_times_six():
+    _, bf16, _ = bench.load_peaks()
+    fp4, _ = bench.fp4_peak_tflops()
+    assert abs(fp4 - bf16 * 6.0) < 1e-6
+
+
+def test_every_benchmark_shape_is_hbm_bound_at_the_peaks():
+    # the algorithmic bytes at the HBM peak outlast the FLOPs at the FP4 peak
+    # for all seven shapes (m=4096: 83 MB vs 120 GFLOP, the C write dominates)
+    for shape in EXPECTED_BYTES:
+        t, bound = bench.shape_floor(*shape)
+        hbm, _, _ = bench.load_peaks()
+        assert bound == "hbm" and abs(t - EXPECTED_BYTES[shape] / (hbm * 1e9)) < 1e-12
+
+
+def test_shape_row_fraction_and_launch_floor_multiple():
+    w = _W(32, 4096, 512, "m32_n4096_k512")
+    row = bench.shape_row(w, [9e-6, 10e-6, 11e-6], {1: 5.0, 2: 7.0}, 152)
     hbm, _, _ = bench.load_peaks()
-    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["kernel"] == "gemm_kernel<32, fused>"
-    per_launch = (bench.algorithmic_bytes(32, 4096, 512) + bench.algorithmic_bytes(32, 2880, 512)) / 2
-    assert r["algorithmic_bytes_per_launch"] == int(per_launch)
-    assert abs(r["achieved"] - per_launch / 9e-6 / 1e9) < 0.01
-    assert abs(r["frac"] - r["achieved"] / hbm) < 1e-4
+    assert row["us_mean"] == 10.0 and row["us_median"] == 10.0
+    assert abs(row["frac"] - EXPECTED_BYTES[(32, 4096, 512)] / (hbm * 1e9) / 10e-6) < 1e-4
+    assert row["launches"] == 1 and row["launch_floor_us"] == 5.0 and row["x_launch_floor"] == 2.0
+    row2 = bench.shape_row(_W(64, 7168, 2048, "m64"), [14e-6], {1: 5.0, 2: 7.0}, 152)
+    assert row2["launches"] == 2 and row2["launch_floor_us"] == 7.0 and row2["x_launch_floor"] == 2.0
+    assert row2["kernels"] == "quant_image_kernel + gemm_kernel<64, image swap>"
 
 
-def test_roofline_of_the_large_gemm_picks_the_longer_floor():
+def test_roofline_picks_the_slowest_call_and_its_floor():
     hbm, bf16, _ = bench.load_peaks()
-    # m = 4096, k = 2048: 83 MB of algorithmic bytes outlast 120 GFLOP at
-    # the peaks (the C write dominates), so the bound is HBM
-    r = bench.dominant_roofline([_W(4096, 7168, 2048)], [[40e-6, 40e-6]], 152)
-    assert r["bound"] == "hbm" and r["kernel"] == "gemm_pair_kernel"
-    assert abs(r["achieved"] - bench.algorithmic_bytes(4096, 7168, 2048) / 40e-6 / 1e9) < 0.01
+    works = [_W(32, 4096, 512, "a"), _W(4096, 7168, 2048, "b")]
+    r = bench.dominant_roofline(works, [[9e-6, 9e-6], [40e-6, 40e-6]], 152)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["shape"] == "b"
+    assert r["kernel"] == "quant_image_kernel + gemm_pair_kernel"
+    assert r["algorithmic_bytes_per_launch"] == EXPECTED_BYTES[(4096, 7168, 2048)]
+    assert abs(r["achieved"] - EXPECTED_BYTES[(4096, 7168, 2048)] / 40e-6 / 1e9) < 0.01
+    assert abs(r["frac"] - r["achieved"] / hbm) < 1e-4
     # a long K makes the FP4 work the longer floor: the measured bf16 peak
     # times the nominal FP4 / bf16 ratio (13.5 / 2.25)
-    r = bench.dominant_roofline([_W(4096, 7168, 16384)], [[100e-6, 100e-6]], 152)
-    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["kernel"] == "gemm_pair_kernel"
+    r = bench.dominant_roofline([_W(4096, 7168, 16384, "c")], [[100e-6, 100e-6]], 152)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
     assert abs(r["peak"] - bf16 * 6) < 0.1
     assert abs(r["achieved"] - 2 * 4096 * 7168 * 16384 / 100e-6 / 1e12) < 0.1
+
+
+def test_oracle_sample_is_bounded():
+    assert bench.sample_of(_W(4096, 7168, 2048)) == (256, 896)
+    assert bench.sample_of(_W(16, 2112, 7168)) == (16, 264)
+    assert bench.sample_of(_W(4, 2880, 512)) == (4, 360)
+
+
+def test_default_workload_is_the_seven_shapes():
+    from precision_bf16_mxfp4_gb300 import inputs
+    names = bench.DEFAULT_WORKLOAD.split(",")
+    assert len(names) == 7 and set(names) == set(inputs.WORKLOADS)
+    assert {(inputs.WORKLOADS[n].m, inputs.WORKLOADS[n].n, inputs.WORKLOADS[n].k) for n in names} == set(EXPECTED_BYTES)
+
+
+def test_host_cpu_reports_cores_and_a_model():
+    cores, model = bench.host_cpu()
+    assert cores >= 1 and isinstance(model, str) and model
 
 
 @pytest.mark.parametrize("m,n,name", [(4, 2880, "gemm_kernel<16, fused>"), (32, 4096, "gemm_kernel<32, fused>"),
