@@ -27,8 +27,22 @@
  *     before anything is enqueued; MXFP4_ERR_CUDA reports a launch failure
  *     (cudaGetLastError right after the launch); faults that happen later
  *     surface at the caller's next synchronization, as with any CUDA call.
- *   - All entry points are reentrant across streams; per-device state is
- *     limited to cached kernel attributes.
+ *   - Entry points may be called from several host threads and on several
+ *     streams at once.  The state the library keeps: per device, cached
+ *     kernel attributes and occupancy figures, and the watchdog flag of
+ *     mxfp4_device_status (a device variable every kernel of the library
+ *     may set); per host thread, the last few tensor maps of C the
+ *     large-m GEMM was launched with; per process, the overrides of
+ *     mxfp4_set_debug_options.  The exception is mxfp4_gemm_noalloc: its
+ *     scratch is one device array shared by every call on a device, so
+ *     calls of it that overlap on the GPU race (see its declaration).
+ *   - Bounded waits and timeouts: every wait inside a GEMM kernel gives up
+ *     after about 2^31 SM clock cycles (~1 s at 2 GHz).  The cycle counter
+ *     keeps running while the context is switched out, so a GPU time-sliced
+ *     with another busy context can reach the limit on a valid call.  A
+ *     kernel that gives up sets the watchdog flag and leaves C undefined
+ *     (partly written); it reports this only through mxfp4_device_status,
+ *     which callers that need to know must call after the GEMM.
  */
 #ifndef MXFP4_H_
 #define MXFP4_H_
@@ -80,7 +94,12 @@ MXFP4_API mxfp4_status mxfp4_quant(const void* a_bf16, int64_t m, int64_t k, int
 
 /*
  * Size in bytes of the prepacked image of an MXFP4 B[n,k] (0 if n <= 0,
- * k <= 0 or k % 32 != 0).
+ * k <= 0 or k % 32 != 0).  The pages hand B to the GEMM already
+ * quantized and shuffled into their kernel's layout (submission 752099,
+ * `custom_kernel` input tuple: B_q and B_shuffle, B_scale); this is the
+ * size of the GB300 form of that pre-shuffled weight: ceil(n/128) x
+ * ceil(k/256) blocks of 17,408 bytes (16 KiB of e2m1 data, 1 KiB of e8m0
+ * scales).
  */
 MXFP4_API size_t mxfp4_prepacked_b_bytes(int64_t n, int64_t k);
 
@@ -103,14 +122,25 @@ MXFP4_API mxfp4_status mxfp4_prepack_b(const void* b_fp4, const void* b_scale, i
 /*
  * Workspace bytes mxfp4_gemm needs for this shape: 0 for m <= 32, where
  * quantized A never leaves shared memory; otherwise the size of A's tiled
- * operand image (the same formula as mxfp4_prepacked_b_bytes(m, k)).
+ * operand image (the same formula as mxfp4_prepacked_b_bytes(m, k)).  The
+ * pages choose by M between quantizing A inside the GEMM and a separate
+ * quantization pass whose output the GEMM reads (submission 739530, v10h
+ * docstring: the fused path for small M, a prequantized A for larger M;
+ * submission 694791, module docstring, "Two kernel paths depending on K");
+ * the workspace holds that intermediate for the second path.  0 also for
+ * invalid arguments.
  */
 MXFP4_API size_t mxfp4_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);
 
 /*
  * mxfp4_gemm -- C[m,n] (row stride ldc) = bf16( quant(A) . B^T ), fp32
  * accumulation; the summation order is unspecified but deterministic for a
- * given shape and device.
+ * given shape and device.  The operation of submission 752099
+ * (`_quant_gemm_fused_launcher`: A quantized with the rule of mxfp4_quant,
+ * then `tl.dot_scaled(a, a_scale, "e2m1", b, b_scale, "e2m1", acc)` with an
+ * fp32 accumulator, stored as `acc.to(bf16)`): every product of two e2m1
+ * values and their two power-of-two scales is exact, so C differs from the
+ * exact sum only by the fp32 summation order and the final rounding.
  *   a_bf16   : bf16 [m, k], row stride lda elements
  *   b_packed : image from mxfp4_prepack_b for (n, k)
  *   c_bf16   : bf16 [m, n], row stride ldc elements (written, not read)
@@ -226,8 +256,9 @@ MXFP4_API mxfp4_status mxfp4_gemm_image(const void* a_image, int64_t m, int64_t 
  *   (mxfp4_gemm_workspace_bytes(m, n, k) > MXFP4_NOALLOC_SCRATCH_BYTES) is
  *   rejected with MXFP4_ERR_WORKSPACE before anything is enqueued.
  *   The first call on a device that needs scratch looks up the array's
- *   device address with that device current (once per device); make that
- *   first call before any stream capture.
+ *   device address with that device current and keeps it (a failed lookup
+ *   is not kept: the next call tries again); make that first call before
+ *   any stream capture.
  *   All calls on a device share the one array: calls that may overlap on
  *   the GPU (unordered streams) race; calls ordered in one stream do not.
  *   Each call rewrites the scratch it uses; nothing needs to start at zero.
@@ -259,6 +290,31 @@ MXFP4_API mxfp4_status mxfp4_measure_fp4_peak(int64_t kblocks_per_sm, double* tf
  * method.  Errors: MXFP4_ERR_INVALID_ARG, MXFP4_ERR_CUDA.
  */
 MXFP4_API mxfp4_status mxfp4_launch_empty(int count, int ctas, void* stream);
+
+/*
+ * mxfp4_set_debug_options -- testing and tuning overrides, process-wide,
+ * for every later call on any thread: split_k forces the number of CTAs the
+ * small-m GEMMs split K over (0 = the planner's own choice, else 1, 2, 4 or
+ * 8, reduced where the shape or the cluster residency does not allow it);
+ * drop_copies = 1 makes the GEMM kernels skip their operand copies (the
+ * large-m kernel: forward no "stage landed" between the CTAs of a pair), so
+ * that their bounded waits run out and the watchdog flag is raised: the
+ * failure-detection path of mxfp4_device_status, exercised without any GPU
+ * fault.  The initial values come from the environment variables
+ * MXFP4_SPLIT_K and MXFP4_DEBUG_DROP_COPIES=1, read once when the library is
+ * loaded.  The pages have no counterpart.  Errors: MXFP4_ERR_INVALID_ARG for
+ * values outside those sets (nothing is changed).
+ */
+MXFP4_API mxfp4_status mxfp4_set_debug_options(int split_k, int drop_copies);
+
+/*
+ * mxfp4_kernel_binary_version -- the binaryVersion (major * 10 + minor) of
+ * the library's GEMM kernel as loaded on the current device: 103 for the
+ * sm_103a code this library is built with.  A diagnostic of the build; the
+ * pages have no counterpart.  Errors: MXFP4_ERR_INVALID_ARG (null version),
+ * MXFP4_ERR_CUDA (the query failed, e.g. no usable device).
+ */
+MXFP4_API mxfp4_status mxfp4_kernel_binary_version(int* version);
 
 /*
  * mxfp4_device_status -- synchronize `stream`, then report and clear the

@@ -30,7 +30,9 @@ from ._lib import (  # noqa: F401  (raw C-ABI names)
     mxfp4_prepack_b_bf16,
     mxfp4_prepacked_b_bytes,
     mxfp4_quant,
+    mxfp4_kernel_binary_version,
     mxfp4_quant_image,
+    mxfp4_set_debug_options,
     mxfp4_status_string,
     mxfp4_version,
 )
@@ -271,6 +273,22 @@ def gemm_noalloc(a, packed: PackedB, out=None):
                             ctypes_void(c.data_ptr()), c.stride(0), _stream_handle(a.device))
     _check(st, "mxfp4_gemm_noalloc")
     return c
+
+
+def set_debug_options(split_k: int = 0, drop_copies: bool = False):
+    """Testing and tuning overrides: force the K split (0 = the planner's
+    choice, else 1, 2, 4 or 8) and make the GEMM kernels drop their operand
+    copies so that their bounded waits run out (failure-detection tests)."""
+    _check(mxfp4_set_debug_options(int(split_k), 1 if drop_copies else 0), "mxfp4_set_debug_options")
+
+
+def kernel_binary_version() -> int:
+    """binaryVersion of the library's GEMM kernel as loaded on the current
+    device (major * 10 + minor: 103 for sm_103a)."""
+    import ctypes
+    v = ctypes.c_int(0)
+    _check(mxfp4_kernel_binary_version(ctypes.byref(v)), "mxfp4_kernel_binary_version")
+    return v.value
 
 
 def device_status(device=None):

@@ -155,6 +155,21 @@ mxfp4_status mxfp4_gemm_image(const void* a_image, int64_t m, int64_t k, const v
                                       static_cast<cudaStream_t>(stream), a_image));
 }
 
+mxfp4_status mxfp4_set_debug_options(int split_k, int drop_copies) {
+  return mxfp4::set_debug_options(split_k, drop_copies) ? MXFP4_OK : MXFP4_ERR_INVALID_ARG;
+}
+
+mxfp4_status mxfp4_kernel_binary_version(int* version) {
+  if (!version) return MXFP4_ERR_INVALID_ARG;
+  const int v = mxfp4::kernel_binary_version();
+  if (v < 0) {
+    (void)cudaGetLastError();
+    return MXFP4_ERR_CUDA;
+  }
+  *version = v;
+  return MXFP4_OK;
+}
+
 mxfp4_status mxfp4_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MXFP4_ERR_CUDA;
   int flag = 0;

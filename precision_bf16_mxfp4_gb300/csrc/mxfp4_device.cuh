@@ -165,4 +165,66 @@ __device__ __forceinline__ void ldg_nc_block(const uint16_t* p, uint4 (&w)[4]) {
   for (int i = 0; i < 4; ++i) w[i] = ldg_nc_v4(p + 8 * i);
 }
 
+// 16 bytes from global memory through L2 (coherent with stores made by other
+// CTAs of the running grid, unlike the read-only path).
+__device__ __forceinline__ uint4 ldg_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// seg / d, in 32-bit arithmetic when every segment index involved fits
+// (a 64-bit division is a long software sequence on the GPU).
+__device__ __forceinline__ int64_t div_seg(int64_t seg, int64_t d, bool small) {
+  return small ? (int64_t)((uint32_t)seg / (uint32_t)d) : seg / d;
+}
+
+// Activation image writer, one warp per row segment: 256 consecutive K
+// elements (8 scale blocks) of one row.  Lane l holds elements 8l..8l+7 (one
+// 16-byte load; the warp reads 512 contiguous bytes), a quad of lanes holds
+// one block and reduces its maximum by shuffles; the warp's 32 four-byte
+// stores fill one swizzled 128-byte row of a data tile and two lanes store
+// the row's scale words (blocks 0-3 and 4-7).  Segment s is row s / kt_count,
+// K block s % kt_count.  The calling warp takes segments lo + first,
+// lo + first + stride, ... below hi, loading kBatch of them before
+// quantizing any so that enough bytes are in flight to cover memory latency.
+// Rows >= m and K beyond k are written as zero codes with scale byte 0.
+// All 32 lanes must call it.
+template <bool kHw, int kBatch>
+__device__ __forceinline__ void quantize_image_segments(const uint16_t* __restrict__ a, int64_t m, int64_t k,
+                                                        int64_t lda, uint8_t* __restrict__ img, int64_t kt_count,
+                                                        int64_t lo, int64_t hi, int64_t first, int64_t stride,
+                                                        int lane) {
+  const bool small = hi + stride * kBatch < (1ll << 31);
+  for (int64_t base = lo + first; base < hi; base += stride * kBatch) {
+    uint4 v[kBatch];
+    int64_t row[kBatch], kt[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int64_t seg = base + (int64_t)i * stride;
+      row[i] = div_seg(seg, kt_count, small);
+      kt[i] = seg - row[i] * kt_count;
+      const int64_t col = kt[i] * kTileK + lane * 8;
+      v[i] = (seg < hi && row[i] < m && col < k) ? ldg_nc_v4(a + row[i] * lda + col) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (base + (int64_t)i * stride >= hi) break;  // uniform across the warp
+      uint32_t sbyte;
+      const uint32_t packed = quantize_quad<kHw>(v[i], sbyte);
+      const int r = (int)(row[i] & (kTileRows - 1));
+      const int b = lane >> 2;
+      uint8_t* tile = img + image_block(row[i] / kTileRows, kt[i], kt_count);
+      *reinterpret_cast<uint32_t*>(tile + tile_data_offset(r, b * 16 + (lane & 3) * 4)) = packed;
+      // scale word of blocks 0-3 (atom 0) and of blocks 4-7 (atom 1): byte b & 3
+      uint32_t word = sbyte << (8 * (b & 3));
+      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 4);
+      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 8);
+      if ((lane & 15) == 0) *reinterpret_cast<uint32_t*>(tile + kTileDataBytes + tile_sf_offset(r, b)) = word;
+    }
+  }
+}
+
 }  // namespace mxfp4

@@ -47,4 +47,12 @@ cudaError_t launch_gemm(const GemmPlan& plan, const void* a_bf16, int64_t m, int
 // Device-side watchdog flag: set by a kernel whose bounded wait ran out.
 cudaError_t read_and_clear_timeout_flag(int* flag);
 
+// Testing and tuning overrides (K split 0/1/2/4/8, copy dropping 0/1);
+// false for values outside those sets.
+bool set_debug_options(int split_k, int drop_copies);
+
+// binaryVersion of the small-m GEMM kernel as loaded on the current device
+// (major * 10 + minor), or -1 if the query failed.
+int kernel_binary_version();
+
 }  // namespace mxfp4

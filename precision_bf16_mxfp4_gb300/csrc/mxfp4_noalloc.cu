@@ -17,7 +17,7 @@
 // it, so nothing in it has to start at zero.
 #include <cuda_runtime.h>
 
-#include <mutex>
+#include <atomic>
 
 #include "mxfp4.h"
 #include "mxfp4_device.cuh"
@@ -30,25 +30,29 @@ constexpr size_t kNoallocScratchBytes = MXFP4_NOALLOC_SCRATCH_BYTES;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_once[kMaxDevices];
-void* g_scratch[kMaxDevices] = {};
-cudaError_t g_setup_error[kMaxDevices] = {};
+std::atomic<void*> g_scratch[kMaxDevices];
 
-// Device address of the scratch array on the current device, looked up once
-// per device while that device is current.  (In host code the array's name
-// only stands for the symbol; it is never a usable device pointer.)
+// Device address of the scratch array on the current device, looked up while
+// that device is current.  (In host code the array's name only stands for the
+// symbol; it is never a usable device pointer.)  Only a successful lookup is
+// kept: a lookup that failed (say, one made during a stream capture) is tried
+// again by the next call.  Two threads that miss at once both look it up and
+// store the same address.
 cudaError_t scratch_on_current_device(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_once[dev], [dev]() {
-    void* p = nullptr;
-    g_setup_error[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    g_scratch[dev] = g_setup_error[dev] == cudaSuccess ? p : nullptr;
-  });
-  if (g_setup_error[dev] != cudaSuccess) return g_setup_error[dev];
-  *out = g_scratch[dev];
+  void* p = g_scratch[dev].load(std::memory_order_acquire);
+  if (!p) {
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+      (void)cudaGetLastError();  // not sticky: the next call tries again
+      return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+    }
+    g_scratch[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
   return cudaSuccess;
 }
 

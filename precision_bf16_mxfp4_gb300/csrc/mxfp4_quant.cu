@@ -25,12 +25,6 @@ constexpr int kQuantSegBatch = 4;  // row segments whose loads one warp keeps in
 // are in flight to cover HBM latency with few registers per thread.
 // Segments are dealt round-robin over all warps of the grid.
 
-// seg / d, in 32-bit arithmetic when every segment index of the grid fits
-// (a 64-bit division is a long software sequence on the GPU).
-__device__ __forceinline__ int64_t div_seg(int64_t seg, int64_t d, bool small) {
-  return small ? (int64_t)((uint32_t)seg / (uint32_t)d) : seg / d;
-}
-
 // bf16 A[m,k] -> packed e2m1 [m,k/2] + e8m0 [m,k/32] (k a multiple of 32).
 template <bool kHw>
 __global__ void __launch_bounds__(kQuantThreads)
@@ -69,9 +63,8 @@ __global__ void __launch_bounds__(kQuantThreads)
 // image, rows >= m as zeros (rows_out = m leaves the last row tile's padding
 // rows untouched: an activation's padding rows only reach accumulator rows
 // that are never stored; a weight image needs them zero).  K beyond k up to
-// the tile edge is written as zeros.  A segment is one 128-byte row of a data
-// tile (the warp's 32 four-byte stores fill it, in swizzled chunk order) and
-// two scale words of the tile's atoms.
+// the tile edge is written as zeros.  Segments are dealt round-robin over
+// every warp of the grid (quantize_image_segments).
 template <bool kHw>
 __global__ void __launch_bounds__(kQuantThreads)
     quant_image_kernel(const uint16_t* __restrict__ a, int64_t m, int64_t k, int64_t lda,
@@ -79,40 +72,11 @@ __global__ void __launch_bounds__(kQuantThreads)
   // Let the dependent GEMM launch now: it prefetches weights and waits for
   // this grid's completion before it reads the image.
   pdl_launch_dependents();
-  const int lane = threadIdx.x & 31;
   const int64_t kt_count = ceil_div(k, kTileK);
-  const int64_t total = rows_out * kt_count;
-  const bool small = total + (int64_t)gridDim.x * kQuantThreads * kQuantSegBatch < (1ll << 31);
   const int64_t warps = (int64_t)gridDim.x * (kQuantThreads / 32);
   const int64_t w0 = (int64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
-  for (int64_t base = w0; base < total; base += warps * kQuantSegBatch) {
-    uint4 v[kQuantSegBatch];
-    int64_t row[kQuantSegBatch], kt[kQuantSegBatch];
-#pragma unroll
-    for (int i = 0; i < kQuantSegBatch; ++i) {
-      const int64_t seg = base + (int64_t)i * warps;
-      row[i] = div_seg(seg, kt_count, small);
-      kt[i] = seg - row[i] * kt_count;
-      const int64_t col = kt[i] * kTileK + lane * 8;
-      // padding rows and K: zero codes, scale byte 0
-      v[i] = (seg < total && row[i] < m && col < k) ? ldg_nc_v4(a + row[i] * lda + col) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int i = 0; i < kQuantSegBatch; ++i) {
-      if (base + (int64_t)i * warps >= total) break;  // uniform across the warp
-      uint32_t sbyte;
-      const uint32_t packed = quantize_quad<kHw>(v[i], sbyte);
-      const int r = (int)(row[i] & (kTileRows - 1));
-      const int b = lane >> 2;
-      uint8_t* tile = img + image_block(row[i] / kTileRows, kt[i], kt_count);
-      *reinterpret_cast<uint32_t*>(tile + tile_data_offset(r, b * 16 + (lane & 3) * 4)) = packed;
-      // scale word of blocks 0-3 (atom 0) and of blocks 4-7 (atom 1): byte b & 3
-      uint32_t word = sbyte << (8 * (b & 3));
-      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 4);
-      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 8);
-      if ((lane & 15) == 0) *reinterpret_cast<uint32_t*>(tile + kTileDataBytes + tile_sf_offset(r, b)) = word;
-    }
-  }
+  quantize_image_segments<kHw, kQuantSegBatch>(a, m, k, lda, img, kt_count, 0, rows_out * kt_count, w0, warps,
+                                               threadIdx.x & 31);
 }
 
 // Linear MXFP4 B (q [n,k/2], scale [n,k/32]) -> tiled image; one thread per

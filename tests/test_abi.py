@@ -44,11 +44,24 @@ def test_library_exports_every_declared_symbol(lib):
         assert getattr(lib, name) is not None
 
 
-def test_library_is_built_for_sm_103a():
-    out = subprocess.run(["cuobjdump", "--list-elf", build.LIB], capture_output=True, text=True)
-    if out.returncode != 0:
-        pytest.skip("cuobjdump unavailable")
-    assert "sm_103a" in out.stdout
+def test_library_is_built_for_sm_103a_only():
+    # every translation unit and the link get exactly one -gencode, for
+    # sm_103a (the GPU tests check the loaded kernel's binaryVersion)
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert not any("arch" in f or "gencode" in f for f in build.FLAGS)
+
+
+def test_debug_options_reject_values_outside_their_sets(lib):
+    assert mx.mxfp4_set_debug_options(3, 0) == _lib.MXFP4_ERR_INVALID_ARG
+    assert mx.mxfp4_set_debug_options(0, 2) == _lib.MXFP4_ERR_INVALID_ARG
+    assert mx.mxfp4_set_debug_options(16, 0) == _lib.MXFP4_ERR_INVALID_ARG
+    for s in (0, 1, 2, 4, 8):
+        assert mx.mxfp4_set_debug_options(s, 0) == _lib.MXFP4_OK
+    assert mx.mxfp4_set_debug_options(0, 0) == _lib.MXFP4_OK
+
+
+def test_binary_version_rejects_a_null_pointer(lib):
+    assert mx.mxfp4_kernel_binary_version(None) == _lib.MXFP4_ERR_INVALID_ARG
 
 
 def test_status_strings_and_version(lib):

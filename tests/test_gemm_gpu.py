@@ -61,26 +61,87 @@ def test_gemm_page_test_shapes_full_output(name):
     assert_close_to_ref(got, _oracle_full(a, bq, bs), what=name)
 
 
-def test_gemm_large_workload_sampled():
+def test_gemm_large_workload_full_output():
+    """m=4096, n=7168, k=2048 (quantizer kernel + CTA-pair GEMM): all 29.4 M
+    outputs against the oracle's definition (fp64 products of the dequantized
+    values, summed by the library matmul), C poisoned with NaN beforehand;
+    a few entries also against the plain oracle loop."""
     name = "m4096_n7168_k2048"
     a, b = inputs.make_inputs(name)
     packed, bq, bs = packed_from_oracle(b)
     got, _ = _run(a, packed, poison=True)
-    assert np.all(np.isfinite(got))
     aq, a_s = oracle.quant(bf16_bits(a))
-    rng = np.random.default_rng(0)
-    rows = np.concatenate([rng.integers(0, a.shape[0], 3000), np.repeat([0, 127, 128, 4095], 64)])
-    cols = np.concatenate([rng.integers(0, b.shape[0], 3000), np.tile(np.arange(0, 7168, 112), 4)])
-    ref = oracle.gemm_entries(aq, a_s, bq, bs, rows, cols)
-    # whole rows and columns through the library matmul on the dequantized values
-    full_rows = [0, 1, 129, 2047, 4095]
-    ref_rows = oracle.dequant(aq[full_rows], a_s[full_rows]) @ oracle.dequant(bq, bs).T
-    full_cols = [0, 255, 256, 7167]
-    ref_cols = oracle.dequant(aq, a_s) @ oracle.dequant(bq[full_cols], bs[full_cols]).T
-    scale = max(np.abs(ref).max(), np.abs(ref_rows).max(), np.abs(ref_cols).max())
-    assert_close_to_ref(got[rows, cols], ref, scale=scale, what="sampled")
-    assert_close_to_ref(got[full_rows], ref_rows, scale=scale, what="rows")
-    assert_close_to_ref(got[:, full_cols], ref_cols, scale=scale, what="cols")
+    ref = oracle.gemm_via_dequant(aq, a_s, bq, bs)
+    assert_close_to_ref(got, ref, what=name)
+    rows = np.array([0, 127, 128, 255, 256, 4095, 2047, 3000])
+    cols = np.array([0, 255, 256, 7167, 128, 129, 4000, 6143])
+    np.testing.assert_allclose(oracle.gemm_entries(aq, a_s, bq, bs, rows, cols), ref[rows, cols], rtol=1e-12)
+
+
+def _selection_weights(n, k, cols):
+    """MXFP4 weights whose row j is 1.0 at K column cols[j] (no entry where
+    cols[j] < 0) and zero elsewhere, every scale 2^0: row j of B^T picks
+    column cols[j] of dequant(quant(A)), so C shows each quantized element."""
+    bq = np.zeros((n, k // 2), np.uint8)
+    for j, c in enumerate(cols):
+        if 0 <= c < k:
+            bq[j, c // 2] = 0x2 if c % 2 == 0 else 0x20  # code 2 = 1.0
+    bs = np.full((n, k // 32), 127, np.uint8)
+    return bq, bs
+
+
+def _quantized_a(a):
+    aq, a_s = oracle.quant(bf16_bits(a))
+    return torch.from_numpy(oracle.dequant(aq, a_s)).to(torch.bfloat16).float().numpy()
+
+
+def test_fused_split4_quantizer_bit_exact_at_k7168():
+    """m=16, n=2112, k=7168 with the wide-exponent, zero-block activation of
+    that workload: the fused kernel with BN = 16 (two quantizer groups taking
+    a stage's K blocks in turn), K split over 4-CTA clusters.  Four launches
+    whose weights select K columns j + 2112 r make every quantized element of
+    A appear in C exactly."""
+    a, _ = inputs.make_inputs("m16_n2112_k7168")
+    m, k, n = 16, 7168, 2112
+    want = _quantized_a(a)
+    for r in range(4):
+        cols = [j + n * r for j in range(n)]
+        bq, bs = _selection_weights(n, k, cols)
+        packed = mx.prepack_b(torch.from_numpy(bq).cuda(), torch.from_numpy(bs).cuda())
+        got, _ = _run(a, packed)
+        for j, c in enumerate(cols):
+            if c < k:
+                np.testing.assert_array_equal(got[:, j], want[:, c], err_msg=f"column {c}")
+            else:
+                assert not np.any(got[:, j])
+
+
+@pytest.mark.parametrize("m", [64, 4096])
+def test_image_quantizer_bit_exact_at_k2048(m):
+    """k=2048 through the activation-image path: m=64 on the swap-AB image
+    kernel (BN = 64), m=4096 (the large workload's activation) on the CTA-pair
+    kernel; an identity weight (n = k) makes C = dequant(quant(A)) exactly."""
+    k = n = 2048
+    a = inputs.make_inputs("m4096_n7168_k2048")[0][:m] if m == 4096 else inputs.make_inputs("m64_n7168_k2048")[0]
+    bq, bs = _selection_weights(n, k, list(range(n)))
+    packed = mx.prepack_b(torch.from_numpy(bq).cuda(), torch.from_numpy(bs).cuda())
+    got, _ = _run(a.contiguous(), packed)
+    np.testing.assert_array_equal(got, _quantized_a(a))
+
+
+@pytest.mark.parametrize("m,n,k,ldb", [(32, 2880, 512, 512), (16, 2112, 7168, 7168), (256, 1500, 2336, 2344),
+                                       (64, 7168, 2048, 2048)])
+def test_prepack_b_bf16_then_gemm_matches_the_oracle(m, n, k, ldb):
+    """The one-call weight path (bf16 B -> prepacked image on the device)
+    followed by mxfp4_gemm, against the oracle's quantization of the same B
+    and the oracle's GEMM."""
+    a = inputs.random_bf16(m, k, seed=m + k)
+    big = torch.zeros((n, ldb), dtype=torch.bfloat16)
+    big[:, :k] = inputs.random_bf16(n, k, seed=n + 7 * k, std=0.05)
+    packed = mx.prepack_b_bf16(big.cuda()[:, :k])
+    got, _ = _run(a, packed, ldc=(n + 7) // 8 * 8)
+    bq, bs = oracle.quant(bf16_bits(big[:, :k]))
+    assert_close_to_ref(got, _oracle_full(a, bq, bs), what=f"{m}x{n}x{k}")
 
 
 @pytest.mark.parametrize("m", [1, 4, 16, 17, 32, 64, 65, 200, 256])
@@ -266,12 +327,20 @@ def test_prepack_roundtrip_through_gemm_columns():
 SPLIT_CASES = [(4, 256, 1024), (16, 300, 2048), (32, 520, 2080), (64, 384, 2048), (200, 256, 2048)]
 
 
+@pytest.fixture
+def forced_split():
+    """Set the planner's K split through mxfp4_set_debug_options; restored after the test."""
+    yield lambda s: mx.set_debug_options(split_k=s)
+    mx.set_debug_options(split_k=0)
+
+
 @pytest.mark.parametrize("split", [1, 2, 4, 8])
 @pytest.mark.parametrize("m,n,k", SPLIT_CASES)
-def test_gemm_every_split_factor(m, n, k, split, monkeypatch):
-    """The planner's K split is overridden (MXFP4_SPLIT_K) to run every cluster
-    size through the reduce-scatter epilogue, including 16-row owners."""
-    monkeypatch.setenv("MXFP4_SPLIT_K", str(split))
+def test_gemm_every_split_factor(m, n, k, split, forced_split):
+    """The planner's K split is overridden (mxfp4_set_debug_options) to run
+    every cluster size through the reduce-scatter epilogue, including 16-row
+    owners."""
+    forced_split(split)
     a = inputs.random_bf16(m, k, seed=m + split)
     b = inputs.random_bf16(n, k, seed=n + split, std=0.3)
     packed, bq, bs = packed_from_oracle(b)
