@@ -294,8 +294,8 @@ MXFP4_API mxfp4_status mxfp4_launch_empty(int count, int ctas, void* stream);
 /*
  * mxfp4_set_debug_options -- testing and tuning overrides, process-wide,
  * for every later call on any thread: split_k forces the number of CTAs the
- * small-m GEMMs split K over (0 = the planner's own choice, else 1, 2, 4 or
- * 8, reduced where the shape or the cluster residency does not allow it);
+ * small-m GEMMs split K over (0 = the planner's own choice, else 1 to 8,
+ * reduced where the shape or the cluster residency does not allow it);
  * drop_copies = 1 makes the GEMM kernels skip their operand copies (the
  * large-m kernel: forward no "stage landed" between the CTAs of a pair), so
  * that their bounded waits run out and the watchdog flag is raised: the

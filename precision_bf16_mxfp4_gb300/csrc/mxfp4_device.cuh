@@ -165,16 +165,6 @@ __device__ __forceinline__ void ldg_nc_block(const uint16_t* p, uint4 (&w)[4]) {
   for (int i = 0; i < 4; ++i) w[i] = ldg_nc_v4(p + 8 * i);
 }
 
-// 16 bytes from global memory through L2 (coherent with stores made by other
-// CTAs of the running grid, unlike the read-only path).
-__device__ __forceinline__ uint4 ldg_cg_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 // seg / d, in 32-bit arithmetic when every segment index involved fits
 // (a 64-bit division is a long software sequence on the GPU).
 __device__ __forceinline__ int64_t div_seg(int64_t seg, int64_t d, bool small) {

@@ -25,12 +25,13 @@
 // operand row tile, so each stage is one bulk copy per row tile: the TMA
 // engine's throughput per SM grows with the size of each copy (about
 // 40 GB/s for 16 KiB copies, 120-160 GB/s for 48-64 KiB ones, measured on
-// GB300), not with the number of copies in flight.  The copies one thread
-// issues are serialized, so each operand stream has its own issuing thread
-// and kFusedSwap spreads its first round of weight stages over four warps.
+// GB300), not with the number of copies in flight.  Each operand stream has
+// its own issuing thread; the weights' first round goes out from thread 0
+// before anything else.
 //
-// K may be split across the S CTAs of a thread-block cluster.  Rank r owns
-// accumulator rows [128r/S, 128(r+1)/S): every rank gathers the rows of its
+// K may be split across the S CTAs (1 <= S <= 8) of a thread-block cluster.
+// Rank r owns accumulator rows [floor(128r/S), floor(128(r+1)/S)) (the ranks
+// own 128/S rows each, give or take one): every rank gathers the rows of its
 // fp32 partial per owner in shared memory (its own rows straight into its
 // slot) and sends each owner its rows as one DSMEM bulk copy into slot r of
 // the owner's reduction buffer, completing on the owner's mbarrier; the owner
@@ -90,8 +91,8 @@ struct Cfg {
   // factors to tensor memory and drain the accumulator.  kFusedSwap: warps
   // 2-9 quantize A, one thread per (row, 32-element block) of a K block;
   // BN = 16 needs only half of them per K block, so the threads form
-  // kQuantGroups groups that take the stage's K blocks in turn; warp 0 issues
-  // the stages after the first round alone
+  // kQuantGroups groups that take the stage's K blocks in turn; thread 0
+  // issues the weights' first round at setup, warp 0 the later stages
   static constexpr int kQuantWarps = kFused ? 8 : 0;
   static constexpr int kQuantGroups = kFused ? 32 / BN : 1;
   // K blocks in a quantizer thread's register ring: two stages' worth for
@@ -124,7 +125,8 @@ struct Cfg {
   // that follows every rank's accumulator.
   static constexpr int kMaxSplit = 8;
   static constexpr int kRedStride = BN + 4;               // fp32 partial-row pitch (floats)
-  static constexpr int kRedBytes = 128 * kRedStride * 4;
+  // S slots of up to ceil(128 / S) rows each: at most 128 + S - 1 rows
+  static constexpr int kRedBytes = (128 + kMaxSplit - 1) * kRedStride * 4;
   static constexpr bool kRedInStages = !kFused;
   static constexpr int kStgPitch = BN + 8;                // elements (kImagePlain)
   static constexpr int kStgBytes = kSwap ? 0 : 128 * kStgPitch * 2;
@@ -229,6 +231,11 @@ __device__ __forceinline__ void store_block_scales(uint32_t taddr, const uint8_t
   const uint32_t v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
   tmem_store_8(taddr, v);
 }
+
+// Accumulator rows of a K split over `split` ranks: rank q owns rows
+// [split_row0(q), split_row0(q + 1)); owner_of(r) is the rank that owns row r.
+__device__ __forceinline__ int split_row0(int q, int split) { return q * kTileRows / split; }
+__device__ __forceinline__ int owner_of(int r, int split) { return ((r + 1) * split - 1) / kTileRows; }
 
 // K steps of 64 in the K block starting at element kt * 256
 __device__ __forceinline__ int k_steps(int64_t k, int64_t kt) {
@@ -355,12 +362,14 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     *abort_flag = 0;
     fence_mbar_init();
     if (split > 1)
-      mbar_arrive_expect_tx(red_full, (uint32_t)((split - 1) * (kTileRows / split) * C::kRedStride * 4));
+      mbar_arrive_expect_tx(red_full, (uint32_t)((split - 1) * (split_row0(rank + 1, split) - split_row0(rank, split)) *
+                                                 C::kRedStride * 4));
     if (!args.drop_copies) {
-      // The weight stream is the long pole: its first round starts now.
-      // kFusedSwap issues stage 0 here and stages 1.. from other warps after
-      // the setup barrier.
-      const int pre = C::kFused ? (nss < 1 ? nss : 1) : (nss < C::kStages ? nss : C::kStages);
+      // The weight stream is the long pole: its whole first round starts
+      // now, before the tensor-memory allocation and the setup barrier (on
+      // GB300 this measured ~0.4 us faster at m = 16, k = 7168 than issuing
+      // stages 1.. from other warps after the barrier).
+      const int pre = nss < C::kStages ? nss : C::kStages;
       for (int i = 0; i < pre; ++i) issue_w(i, i);
     }
   }
@@ -372,8 +381,6 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (C::kFused && lane == 0 && warp >= 2 && warp - 1 < C::kStages && warp - 1 < nss && !args.drop_copies)
-    issue_w(warp - 1, warp - 1);  // stage i = warp - 1 of the first round, one issuing warp each
   // the owners' reduction barriers must be initialized before any rank arrives on them
   if (split > 1) cluster_arrive_relaxed();
 
@@ -539,8 +546,9 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   //        idle once the accumulator is done.
   float* red = reinterpret_cast<float*>(smem + C::kOffRed);
   __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem);
-  const int rows_per_rank = kTileRows / split;
-  const int row_lo = rank * rows_per_rank;  // first accumulator row this CTA stores
+  const int slot_rows = (kTileRows + split - 1) / split;  // pitch of the per-owner slots (rows)
+  const int row_lo = split_row0(rank, split);             // first accumulator row this CTA stores
+  const int my_rows = split_row0(rank + 1, split) - row_lo;
   __syncwarp();
   if (split > 1) cluster_wait();  // every rank's barriers are initialized
   // Warps 2-5 drain the accumulator, warp w reading tensor-memory lane
@@ -551,16 +559,16 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     const int quad = warp & 3;
     const int col_lo = ((warp - 2) >> 2) * C::kEpiCols;
     const int row = quad * 32 + lane;  // accumulator row = tensor-memory lane
-    const int owner = row / rows_per_rank;  // a warp's rows span two owners when each owns 16
+    const int owner = owner_of(row, split);  // a warp's rows can span two owners
     const int64_t n_swap = a_tile * kTileRows + row;
     const bool ok = wait_bounded(accum, 0, abort_flag);
     tc_fence_after();
     // split: this rank's own rows go to its slot of `red`; the rows another
     // rank owns are gathered per owner in the (idle) stage buffers and sent
     // below as one bulk copy per owner
-    float* part = (owner == rank ? red + (size_t)rank * rows_per_rank * C::kRedStride
-                                 : reinterpret_cast<float*>(smem + C::kOffOut) + (size_t)owner * rows_per_rank * C::kRedStride) +
-                  (size_t)(row - owner * rows_per_rank) * C::kRedStride;
+    float* part = (owner == rank ? red + (size_t)rank * slot_rows * C::kRedStride
+                                 : reinterpret_cast<float*>(smem + C::kOffOut) + (size_t)owner * slot_rows * C::kRedStride) +
+                  (size_t)(row - split_row0(owner, split)) * C::kRedStride;
     constexpr int kChunk = C::kEpiCols >= 32 ? 32 : 16;
 #pragma unroll 1
     for (int c0 = col_lo; c0 < col_lo + C::kEpiCols; c0 += kChunk) {
@@ -616,25 +624,25 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     // --------------- reduce-scatter: slot `rank` of every other owner's `red`
     // (in the owners' stage buffers: every rank's accumulator must be complete)
     if (C::kRedInStages) cluster_sync();
-    const uint32_t slot_bytes = (uint32_t)(rows_per_rank * C::kRedStride * 4);
     if (threadIdx.x == 0 && !*abort_flag) {
       for (int o = 0; o < split; ++o) {
         if (o == rank) continue;
-        bulk_copy_to_cluster(map_cluster(smem_addr(red + (size_t)rank * rows_per_rank * C::kRedStride), (uint32_t)o),
-                             reinterpret_cast<const float*>(smem + C::kOffOut) + (size_t)o * rows_per_rank * C::kRedStride,
-                             slot_bytes, map_cluster(smem_addr(red_full), (uint32_t)o));
+        const uint32_t bytes = (uint32_t)((split_row0(o + 1, split) - split_row0(o, split)) * C::kRedStride * 4);
+        bulk_copy_to_cluster(map_cluster(smem_addr(red + (size_t)rank * slot_rows * C::kRedStride), (uint32_t)o),
+                             reinterpret_cast<const float*>(smem + C::kOffOut) + (size_t)o * slot_rows * C::kRedStride,
+                             bytes, map_cluster(smem_addr(red_full), (uint32_t)o));
       }
       bulk_commit_group();
     }
     // ------------------------- sum this rank's rows over the S partials, in rank order
     wait_bounded_cluster(red_full, 0, abort_flag);  // the other ranks' rows have landed
     constexpr int kC4 = BN / 4;
-    for (int g = threadIdx.x; g < rows_per_rank * kC4; g += C::kThreads) {
-      const int rr = g % rows_per_rank, c4 = g / rows_per_rank;
+    for (int g = threadIdx.x; g < my_rows * kC4; g += C::kThreads) {
+      const int rr = g % my_rows, c4 = g / my_rows;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int q = 0; q < split; ++q) {
         const float4 v =
-            *reinterpret_cast<const float4*>(red + (size_t)(q * rows_per_rank + rr) * C::kRedStride + c4 * 4);
+            *reinterpret_cast<const float4*>(red + (size_t)(q * slot_rows + rr) * C::kRedStride + c4 * 4);
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
@@ -668,7 +676,7 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     const int64_t m0 = a_tile * kTileRows;
     const int64_t n0 = b_tile * BN;
     constexpr int nch = BN / 8;
-    for (int idx = threadIdx.x; idx < rows_per_rank * nch; idx += C::kThreads) {
+    for (int idx = threadIdx.x; idx < my_rows * nch; idx += C::kThreads) {
       const int r = row_lo + idx / nch, ch = idx % nch;
       const int64_t mi = m0 + r;
       const int64_t n = n0 + ch * 8;
@@ -1123,7 +1131,7 @@ int num_sms() {
 }
 
 // Testing and tuning overrides: the K-split factor the planner picks
-// (0 = its own choice, else 1, 2, 4 or 8, clamped to what the shape and the
+// (0 = its own choice, else 1 to 8, clamped to what the shape and the
 // kernel allow) and the copy-dropping hook of the failure-detection test.
 // Read from MXFP4_SPLIT_K and MXFP4_DEBUG_DROP_COPIES once, when the library
 // is loaded, and changed afterwards only through set_debug_options: no call
@@ -1131,7 +1139,7 @@ int num_sms() {
 static int env_split() {
   const char* v = getenv("MXFP4_SPLIT_K");
   const int s = v ? atoi(v) : 0;
-  return (s == 1 || s == 2 || s == 4 || s == 8) ? s : 0;
+  return (s >= 1 && s <= 8) ? s : 0;
 }
 static int env_drop() {
   const char* v = getenv("MXFP4_DEBUG_DROP_COPIES");
@@ -1143,7 +1151,7 @@ static std::atomic<int> g_drop_copies{env_drop()};
 static int split_override() { return g_split_override.load(std::memory_order_relaxed); }
 
 bool set_debug_options(int split_k, int drop_copies) {
-  if (!(split_k == 0 || split_k == 1 || split_k == 2 || split_k == 4 || split_k == 8)) return false;
+  if (split_k < 0 || split_k > 8) return false;
   if (drop_copies != 0 && drop_copies != 1) return false;
   g_split_override.store(split_k, std::memory_order_relaxed);
   g_drop_copies.store(drop_copies, std::memory_order_relaxed);
@@ -1169,10 +1177,19 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan, bool a_image
     const int s_max = 8;  // the kernels' kMaxSplit
     // The cluster exchange of a split costs about 1-1.5 us (measured on
     // GB300 for m <= 64); a 256-K block of weights streams in a fraction of
-    // that, so a split pays only while every rank keeps several K blocks:
-    // k = 512 and 2048 run unsplit, k = 7168 with n = 2112 splits 4 ways.
+    // that, so a split pays only while every rank keeps several K blocks.
+    // The fused kernel (m <= 32) streams only weights, and the rate at which
+    // one SM receives them is what bounds it after an L2 flush, so it takes
+    // the most ranks that fit on the SMs with at least 4 K blocks each
+    // (k = 7168 with n = 2112: 6 ranks, 102 CTAs); the image kernels keep
+    // power-of-two splits with at least 5 K blocks per rank (k = 512 and
+    // 2048 run unsplit).
     int s = 1;
-    while (s < s_max && p.grid_x * s * 2 <= sms && KT / (s * 2) >= 5) s *= 2;
+    if (p.mode == kFusedSwap) {
+      while (s < s_max && p.grid_x * (s + 1) <= sms && KT >= 4 * (s + 1)) ++s;
+    } else {
+      while (s < s_max && p.grid_x * s * 2 <= sms && KT / (s * 2) >= 5) s *= 2;
+    }
     if (forced) s = forced <= KT ? forced : 1;
     p.split = s;
     p.grid_y = s;
@@ -1210,10 +1227,10 @@ int make_gemm_plan(int64_t m, int64_t n, int64_t k, GemmPlan* plan, bool a_image
 template <int BN, int kMode>
 static int max_resident_clusters(int split) {
   using C = Cfg<BN, kMode>;
-  static std::atomic<int> cache[64][4];  // [device][log2 split - 1]
+  static std::atomic<int> cache[64][9];  // [device][split]
   int dev = 0;
   cudaGetDevice(&dev);
-  const int idx = split == 2 ? 0 : split == 4 ? 1 : split == 8 ? 2 : 3;
+  const int idx = split >= 0 && split <= 8 ? split : 0;
   if (dev < 0 || dev >= 64) return 0;
   const int hit = cache[dev][idx].load(std::memory_order_relaxed);
   if (hit != 0) return hit;
@@ -1253,14 +1270,15 @@ static cudaError_t launch_one(const GemmPlan& plan_in, const GemmArgs& args_in, 
     attr_done[dev].store(true, std::memory_order_relaxed);
   }
   // A K split whose clusters cannot all be resident at once would run in two
-  // waves; halve it until they fit (the result does not depend on the split).
+  // waves; reduce it until they fit (the result does not depend on the split
+  // beyond the fp32 summation order).
   GemmPlan plan = plan_in;
   GemmArgs args = args_in;
   while (plan.split > 1) {
     const int fit = max_resident_clusters<BN, kMode>(plan.split);
     if (fit < 0 || (int64_t)fit * plan.split >= plan.grid_x * plan.grid_y) break;
-    plan.grid_y = plan.grid_y / plan.split * (plan.split / 2);
-    plan.split /= 2;
+    plan.grid_y = plan.grid_y / plan.split * (plan.split - 1);
+    plan.split -= 1;
   }
   args.split = plan.split;
   cudaLaunchConfig_t cfg{};

@@ -334,12 +334,13 @@ def forced_split():
     mx.set_debug_options(split_k=0)
 
 
-@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("split", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("m,n,k", SPLIT_CASES)
 def test_gemm_every_split_factor(m, n, k, split, forced_split):
     """The planner's K split is overridden (mxfp4_set_debug_options) to run
-    every cluster size through the reduce-scatter epilogue, including 16-row
-    owners."""
+    every cluster size through the reduce-scatter epilogue: owners of 16
+    rows (split 8) and uneven owners (splits 3, 5, 6, 7: 42-43, 25-26, 21-22
+    and 18-19 rows)."""
     forced_split(split)
     a = inputs.random_bf16(m, k, seed=m + split)
     b = inputs.random_bf16(n, k, seed=n + split, std=0.3)
@@ -489,3 +490,32 @@ def test_pair_kernel_more_tiles_than_pairs_and_missing_row_tile():
     got, c_full = _run(a, packed, ldc=n + 16)
     assert_close_to_ref(got, _oracle_full(a, bq, bs), what="pair kernel, 95 tiles")
     assert torch.isnan(c_full[:, n:]).all()
+
+
+@pytest.mark.parametrize("m,n,k", [(16, 2112, 7168), (64, 7168, 2048), (256, 3072, 1536), (4096, 7168, 2048)])
+def test_gemm_in_a_captured_cuda_graph(m, n, k):
+    """mxfp4_gemm captured into a CUDA graph (for m > 32 the quantization
+    kernel and the GEMM as its programmatic dependent) and replayed on new
+    contents of the same A buffer gives what the eager call gives."""
+    packed, _, _ = packed_from_oracle(inputs.random_bf16(n, k, seed=n + k, std=0.1))
+    a = torch.empty((m, k), dtype=torch.bfloat16, device="cuda")
+    c = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(mx.workspace_bytes(m, n, k), 16), dtype=torch.uint8, device="cuda")
+    a.copy_(inputs.random_bf16(m, k, seed=1))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        mx.gemm(a, packed, out=c, workspace=ws)  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        mx.gemm(a, packed, out=c, workspace=ws)
+    for seed in (2, 3):
+        a.copy_(inputs.random_bf16(m, k, seed=seed))
+        g.replay()
+        torch.cuda.synchronize()
+        want = mx.gemm(a, packed)
+        torch.cuda.synchronize()
+        assert torch.equal(c.view(torch.int16), want.view(torch.int16)), f"replay with seed {seed}"
+    mx.device_status()
