@@ -133,6 +133,7 @@ struct Cfg {
   static constexpr int kOffOut = (kStgBytes + 1023) & ~1023;
   static constexpr int kOffRed = kRedInStages ? kOffOut + ((kRedBytes + 1023) & ~1023) : (kOffMisc + 16 + 15) & ~15;
   static_assert(kOffOut + kRedBytes <= kOffBars, "the gather buffer must fit in the stage buffers");
+  static_assert(!kSwap || BN * (kTileRows + 8) * 2 <= kOffBars, "the swap-AB output rows must fit in the stage buffers");
   static_assert(!kRedInStages || kOffRed + kRedBytes <= kOffBars, "epilogue buffers must fit in the stage buffers");
   static constexpr int kSmemBytes = (kRedInStages ? kOffMisc + 16 : kOffRed + kRedBytes) + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -542,10 +543,12 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
   // ------------------------------------------------------------- epilogue
   //   red: [S][128/S][kRedStride] fp32 rows this rank owns, pushed by rank q
   //        into slot q (a split cluster);
-  //   stg: bf16 output tile [128][BN+8] (kImagePlain), in the stage buffers,
-  //        idle once the accumulator is done.
+  //   stg: bf16 output tile in the stage buffers, idle once the accumulator
+  //        is done: [128][BN+8] (kImagePlain), or C's rows [BN][128+8]
+  //        (swap-AB, unsplit).
   float* red = reinterpret_cast<float*>(smem + C::kOffRed);
   __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem);
+  constexpr int kSwapPitch = kTileRows + 8;  // elements: 272-byte rows, 16-byte aligned
   const int slot_rows = (kTileRows + split - 1) / split;  // pitch of the per-owner slots (rows)
   const int row_lo = split_row0(rank, split);             // first accumulator row this CTA stores
   const int my_rows = split_row0(rank + 1, split) - row_lo;
@@ -560,7 +563,6 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
     const int col_lo = ((warp - 2) >> 2) * C::kEpiCols;
     const int row = quad * 32 + lane;  // accumulator row = tensor-memory lane
     const int owner = owner_of(row, split);  // a warp's rows can span two owners
-    const int64_t n_swap = a_tile * kTileRows + row;
     const bool ok = wait_bounded(accum, 0, abort_flag);
     tc_fence_after();
     // split: this rank's own rows go to its slot of `red`; the rows another
@@ -587,18 +589,12 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
               __uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
       } else if (C::kSwap) {
         // accumulator row = C column n, accumulator column = C row: the
-        // warp's 32 lanes store 32 consecutive columns of each C row
-        if (n_swap < args.n) {
-          __nv_bfloat16* p = args.c + (int64_t)c0 * args.ldc + n_swap;
-          if (c0 + kChunk <= args.m) {
+        // values go to shared memory as C rows (the warp's 32 lanes fill 32
+        // consecutive columns of each row) and are stored below as 16-byte
+        // pieces of whole rows
+        __nv_bfloat16* p = stg + (size_t)c0 * kSwapPitch + row;
 #pragma unroll
-            for (int j = 0; j < kChunk; ++j, p += args.ldc) *p = __float2bfloat16_rn(__uint_as_float(r[j]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < kChunk; ++j, p += args.ldc)
-              if (c0 + j < args.m) *p = __float2bfloat16_rn(__uint_as_float(r[j]));
-          }
-        }
+        for (int j = 0; j < kChunk; ++j) p[j * kSwapPitch] = __float2bfloat16_rn(__uint_as_float(r[j]));
       } else {
 #pragma unroll
         for (int j = 0; j < kChunk; j += 8) {
@@ -612,6 +608,25 @@ __global__ void __launch_bounds__(Cfg<BN, kMode>::kThreads, 1) gemm_kernel(const
       }
     }
     if (split > 1) fence_proxy_async_smem();  // the gathered rows are read by bulk copies
+    if (C::kSwap && split == 1) {
+      // C rows [0, min(m, BN)) of this tile's 128 columns from shared memory:
+      // 16 lanes per 256-byte row, 16 bytes each (8 columns)
+      named_barrier_sync(1, C::kEpiWarps * 32);
+      const int64_t n0 = a_tile * kTileRows;
+      const int rows = args.m < BN ? (int)args.m : BN;
+      for (int idx = (int)threadIdx.x - 64; idx < rows * (kTileRows / 8); idx += C::kEpiWarps * 32) {
+        const int mr = idx >> 4, ch = idx & 15;
+        const int64_t n = n0 + ch * 8;
+        if (!ok || n >= args.n) continue;
+        const __nv_bfloat16* src = stg + (size_t)mr * kSwapPitch + ch * 8;
+        __nv_bfloat16* dst = args.c + (int64_t)mr * args.ldc + n;
+        if (n + 8 <= args.n) {
+          *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+        } else {
+          for (int e = 0; e < 8 && n + e < args.n; ++e) dst[e] = src[e];
+        }
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
