@@ -99,8 +99,11 @@ __device__ __forceinline__ uint32_t e2m1x2_hw(float lo, float hi) {
 
 // Encode 8 consecutive bf16 values (K order: w.x low half first) with the
 // block's inverse scale into 4 bytes of packed e2m1 (byte i holds elements
-// 2i and 2i+1).  Signs come from the inputs, so values that round to zero
-// keep their sign (0x8 for negatives).
+// 2i and 2i+1).  Values that round to zero keep their sign (0x8 for
+// negatives): the hardware conversion does so itself (on GB300 it gives 0x8
+// for a negative input that rounds to zero; the GPU tests check every bf16
+// value under every block exponent), the comparison encoder takes the signs
+// from the inputs.
 template <bool kHardwareCvt>
 __device__ __forceinline__ uint32_t encode8(const uint4& w, float inv_scale) {
   const uint32_t words[4] = {w.x, w.y, w.z, w.w};
@@ -115,8 +118,8 @@ __device__ __forceinline__ uint32_t encode8(const uint4& w, float inv_scale) {
       byte = e2m1x2_hw(x0, x1) & 0xFFu;
     } else {
       byte = e2m1_code_sw(fabsf(x0)) | (e2m1_code_sw(fabsf(x1)) << 4);
+      byte |= ((v >> 12) & 0x8u) | ((v >> 24) & 0x80u);  // input signs -> bits 3 and 7
     }
-    byte |= ((v >> 12) & 0x8u) | ((v >> 24) & 0x80u);  // input signs -> bits 3 and 7
     out |= byte << (8 * i);
   }
   return out;
