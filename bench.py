@@ -383,6 +383,7 @@ def run_ours(args, names, rank, world, local_rank):
     mx.device_status(dev)
     # the last timed output still matches the first (checked) one bit for bit
     repeat_ok = all(np.array_equal(s["c"].float().cpu().numpy(), s["c_first"]) for s in shapes)
+    host_us = host_call_overhead(mx, shapes, stream)
 
     # the dominant call's two kernels timed alone (outside the step), for the
     # roofline's split: the GEMM on a ready activation image, and the
@@ -451,10 +452,42 @@ def run_ours(args, names, rank, world, local_rank):
         "roofline": roofline,
         "clocks": clk.summary(),
         "repeat_bit_identical": repeat_ok,
+        "host_us_per_call": host_us,
         "wall_s_timed_region": round(wall, 4),
     }
     if baseline:
         out["cpu_baseline"] = baseline
+    return out
+
+
+def host_call_overhead(mx, shapes, stream, calls=200):
+    """Host time per mxfp4_gemm call through the raw C ABI (arguments
+    prebuilt, no synchronization inside the loop: the enqueue cost a caller
+    pays), per shape, in microseconds; the ctypes call itself is included."""
+    import ctypes
+    import torch
+    lib = mx._lib.load()
+    P = ctypes.c_void_p
+    out = {}
+    for s in shapes:
+        w = s["w"]
+        ws = s["ws"]
+        argv = (P(s["a"].data_ptr()), w.m, w.k, s["a"].stride(0), P(s["packed"].buf.data_ptr()), w.n,
+                P(s["c"].data_ptr()), s["c"].stride(0), P(ws.data_ptr() if ws is not None else 0),
+                ws.numel() if ws is not None else 0, P(stream.cuda_stream))
+        for _ in range(5):
+            lib.mxfp4_gemm(*argv)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(calls):
+            lib.mxfp4_gemm(*argv)
+        dt = time.perf_counter() - t0
+        torch.cuda.synchronize()
+        out[w.name] = round(dt / calls * 1e6, 2)
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        lib.mxfp4_version()
+    out["ctypes_call_floor"] = round((time.perf_counter() - t0) / calls * 1e6, 2)
     return out
 
 
