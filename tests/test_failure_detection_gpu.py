@@ -22,12 +22,12 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("m,n,k,split", [(8, 256, 1024, "1"), (16, 256, 1024, "4"), (48, 256, 1024, "2"),
-                                         (1024, 4864, 256, "1")])
+                                         (1024, 4864, 256, "1"), (1024, 4864, 2304, "1")])
 def test_wait_timeout_is_reported_and_recoverable(m, n, k, split):
-    """(1024, 4864, 256): 152 output tiles of 128 x 256 select the CTA-pair
-    kernel, whose odd CTAs then forward no "stage landed": the even CTAs'
-    MMA waits run out, both CTAs of every pair wind down and meet at their
-    final cluster barrier."""
+    """(1024, 4864, 256) and (1024, 4864, 2304): 152 output tiles of 128 x 256
+    select the CTA-pair kernel (one and five stages per tile), whose odd CTAs
+    then forward no "stage landed": the even CTAs' MMA waits run out, both
+    CTAs of every pair wind down and meet at their final cluster barrier."""
     a = inputs.random_bf16(m, k, seed=m)
     b = inputs.random_bf16(n, k, seed=n, std=0.3)
     packed, bq, bs = packed_from_oracle(b)

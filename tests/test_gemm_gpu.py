@@ -519,3 +519,18 @@ def test_gemm_in_a_captured_cuda_graph(m, n, k):
         torch.cuda.synchronize()
         assert torch.equal(c.view(torch.int16), want.view(torch.int16)), f"replay with seed {seed}"
     mx.device_status()
+
+
+@pytest.mark.parametrize("m,n,k", [(1024, 4864, 2560), (1100, 4856, 2016), (4096, 2048, 256), (2048, 4096, 1024)])
+def test_pair_kernel_long_k_tails_and_tile_rounds(m, n, k):
+    """The CTA-pair plan on long K (2560: ten K blocks, five stages per
+    tile), a K tail inside the last stage (2016 = 7.875 K blocks) with a
+    missing odd activation row tile and a partial column tile (1100 x 4856),
+    more tiles than pairs with the ring running across tiles (4096 x 2048 x
+    256: 128 tiles over 76 pairs), and 2048 x 4096 x 1024."""
+    a = inputs.random_bf16(m, k, seed=m + n + k)
+    b = inputs.random_bf16(n, k, seed=n + 11 * k, std=0.3)
+    packed, bq, bs = packed_from_oracle(b)
+    got, c_full = _run(a, packed, ldc=n + 8)
+    assert_close_to_ref(got, _oracle_full(a, bq, bs), what=f"{m}x{n}x{k}")
+    assert torch.isnan(c_full[:, n:]).all(), "wrote outside the [m, n] window"
