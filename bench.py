@@ -99,19 +99,22 @@ def source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_key):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+def profiled_traffic(shape_name, launches=None):
+    """DRAM bytes (read + write) of one call on `shape_name`, summed over the
+    call's kernels from the committed ncu captures, if they were taken on the
+    current kernel sources and cover every kernel of the call; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
-        entry = t[kernel_key]
-        if entry.get("source_hash") == source_hash():
-            return int(entry["dram_bytes_per_launch"])
+        if t.get("source_hash") != source_hash():
+            return None
+        kernels = t["shapes"][shape_name]["kernels"]
+        if launches is not None and len(kernels) != launches:
+            return None
+        return int(sum(v["dram_read"] + v["dram_write"] for v in kernels.values()))
     except Exception:
-        pass
-    return None
+        return None
 
 
 def host_cpu():
@@ -215,7 +218,8 @@ def shape_row(w, times_s, floors_us, sms):
            "launches": launches_per_gemm(w.m),
            "us_mean": round(mean * 1e6, 3), "us_median": round(med * 1e6, 3),
            "tbps": round(byt / mean / 1e12, 4), "tflops": round(fl / mean / 1e12, 3),
-           "bound": bound, "floor_us": round(floor_s * 1e6, 3), "frac": round(floor_s / mean, 4)}
+           "bound": bound, "floor_us": round(floor_s * 1e6, 3), "frac": round(floor_s / mean, 4),
+           "algorithmic_bytes": int(byt), "traffic": profiled_traffic(w.name, launches_per_gemm(w.m))}
     if floors_us:
         lf = floors_us.get(launches_per_gemm(w.m))
         if lf:
@@ -241,9 +245,7 @@ def dominant_roofline(works, dev_times, sms, extra=None):
     fl, byt = flops(w.m, w.n, w.k), algorithmic_bytes(w.m, w.n, w.k)
     _, bound = shape_floor(w.m, w.n, w.k)
     kernel = call_kernels(w.m, w.n, sms)
-    key = {(32, 4096, 512): "gemm_fused_bn32", (32, 2880, 512): "gemm_fused_bn32",
-           (4096, 7168, 2048): "gemm_pair_m4096"}.get((w.m, w.n, w.k))
-    traffic = profiled_traffic(key) if key else None
+    traffic = profiled_traffic(w.name, launches_per_gemm(w.m))
     out = {"bound": bound, "kernel": kernel, "shape": w.name,
            "traffic": traffic, "timed": "CUDA events around the whole call on its stream, mean over the timed steps"}
     if bound == "tensor":

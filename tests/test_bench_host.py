@@ -5,6 +5,7 @@ from __future__ import annotations
 
 import io
 import json
+import os
 import socket
 from contextlib import redirect_stdout
 
@@ -96,7 +97,19 @@ def test_clock_summary_flags_throttle_reasons():
 
 
 def test_traffic_is_reported_only_for_the_profiled_sources():
-    assert bench.profiled_traffic("no_such_kernel") is None
+    assert bench.profiled_traffic("no_such_shape") is None
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        t = json.load(f)
+    for name, entry in t["shapes"].items():
+        m = int(name.split("_")[0][1:])
+        kernels = entry["kernels"]
+        assert len(kernels) == bench.launches_per_gemm(m), name
+        total = sum(v["dram_read"] + v["dram_write"] for v in kernels.values())
+        got = bench.profiled_traffic(name, bench.launches_per_gemm(m))
+        # the captured figure, or nothing once the kernel sources have changed
+        assert got == (total if t["source_hash"] == bench.source_hash() else None)
+        # a call with another number of kernels is never given this capture
+        assert bench.profiled_traffic(name, bench.launches_per_gemm(m) + 1) is None
 
 
 class _W:
