@@ -225,6 +225,10 @@ def shape_row(w, times_s, floors_us, sms):
         if lf:
             row["launch_floor_us"] = lf
             row["x_launch_floor"] = round(mean * 1e6 / lf, 3)
+        mf = floors_us.get(("minimal", launches_per_gemm(w.m)))
+        if mf:
+            row["minimal_floor_us"] = mf
+            row["x_minimal_floor"] = round(mean * 1e6 / mf, 3)
     return row
 
 
@@ -290,11 +294,15 @@ def event_time(stream, flush, fn, reps, warmup=3):
 
 
 def measure_launch_floor_live(dev, stream, flush, mx, reps):
-    """Event time of one and of two empty kernels after the same flush (us)."""
+    """Event time (us) of one and of two empty kernels after the same flush,
+    and of one and two minimal kernels (a global read, a tensor-memory
+    allocation and a global write per CTA: the least a GEMM launch does)."""
     out = {}
     for count in (1, 2):
         mean, med = event_time(stream, flush, lambda: mx.launch_empty(count, 32, dev), reps)
         out[count] = (round(mean * 1e6, 3), round(med * 1e6, 3))
+        mean, med = event_time(stream, flush, lambda: mx.launch_minimal(count, 32, dev), reps)
+        out[("minimal", count)] = (round(mean * 1e6, 3), round(med * 1e6, 3))
     return out
 
 
@@ -443,8 +451,14 @@ def run_ours(args, names, rank, world, local_rank):
                   "fp4_nominal_tflops": NOMINAL_FP4_TFLOPS},
         "launch_floor": {"1_kernel_us": {"mean": floors[1][0], "median": floors[1][1]},
                          "2_kernel_us": {"mean": floors[2][0], "median": floors[2][1]},
-                         "method": "mxfp4_launch_empty (32 CTAs) between the same events after the same flush, "
-                                   f"{reps} repetitions"},
+                         "1_minimal_kernel_us": {"mean": floors[("minimal", 1)][0],
+                                                 "median": floors[("minimal", 1)][1]},
+                         "2_minimal_kernel_us": {"mean": floors[("minimal", 2)][0],
+                                                 "median": floors[("minimal", 2)][1]},
+                         "method": "mxfp4_launch_empty (32 empty CTAs) and mxfp4_launch_minimal (32 CTAs that "
+                                   "each read a word, allocate and free tensor memory and write a word) between "
+                                   f"the same events after the same flush, {reps} repetitions; shapes carry "
+                                   "x_launch_floor (empty) and x_minimal_floor"},
         "e2e": {"value": round(world * step_bytes / e2e_s / 1e12, 5), "unit": "TB/s",
                 "us_per_step": round(e2e_s * 1e6, 3),
                 "h2d_bytes_per_step": int(sum(s["a_host"].numel() * 2 for s in shapes)),
@@ -656,9 +670,11 @@ def measure_fp4_peak(local_rank, kblocks_per_sm=4000, runs=5):
 
 
 def measure_launch_floor(local_rank, steps, warmup, ctas=32):
-    """The launch floor of the small-m GEMMs: CUDA events around one empty
-    kernel, and around two back to back, each after the same L2 flush the
-    GEMMs get (mean and median over `steps`, in microseconds)."""
+    """The launch floors of the small-m GEMMs: CUDA events around one empty
+    kernel and around two back to back, and the same for minimal kernels
+    (a global read, a tensor-memory allocation and a global write per CTA),
+    each after the same L2 flush the GEMMs get (mean and median over
+    `steps`, in microseconds)."""
     import torch
 
     import precision_bf16_mxfp4_gb300 as mx
@@ -671,6 +687,8 @@ def measure_launch_floor(local_rank, steps, warmup, ctas=32):
     for count in (1, 2):
         mean, med = event_time(stream, flush, lambda: mx.launch_empty(count, ctas, dev), steps, warmup)
         out[f"{count}_kernel_us"] = {"mean": round(mean * 1e6, 3), "median": round(med * 1e6, 3)}
+        mean, med = event_time(stream, flush, lambda: mx.launch_minimal(count, ctas, dev), steps, warmup)
+        out[f"{count}_minimal_kernel_us"] = {"mean": round(mean * 1e6, 3), "median": round(med * 1e6, 3)}
     return out
 
 

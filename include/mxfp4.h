@@ -292,6 +292,19 @@ MXFP4_API mxfp4_status mxfp4_measure_fp4_peak(int64_t kblocks_per_sm, double* tf
 MXFP4_API mxfp4_status mxfp4_launch_empty(int count, int ctas, void* stream);
 
 /*
+ * mxfp4_launch_minimal -- enqueue `count` (1..16) minimal kernels of `ctas`
+ * (1..65535) 32-thread CTAs on `stream`: each CTA reads one word of a
+ * library-owned device array, allocates and frees 32 tensor-memory columns
+ * and writes one word of the same array.  That is the least any GEMM launch
+ * does, and after an L2 flush by writes each of the three costs a kernel
+ * about as much event time as the empty kernel's whole launch overhead, so
+ * this is the floor a tcgen05 GEMM can meet.  Overlapping calls race on the
+ * array, harmlessly (its values are never read by anything else).
+ * Errors: MXFP4_ERR_INVALID_ARG, MXFP4_ERR_CUDA.
+ */
+MXFP4_API mxfp4_status mxfp4_launch_minimal(int count, int ctas, void* stream);
+
+/*
  * mxfp4_set_debug_options -- testing and tuning overrides, process-wide,
  * for every later call on any thread: split_k forces the number of CTAs the
  * small-m GEMMs split K over (0 = the planner's own choice, else 1 to 8,

@@ -25,6 +25,7 @@ from ._lib import (  # noqa: F401  (raw C-ABI names)
     mxfp4_gemm_noalloc,
     mxfp4_gemm_workspace_bytes,
     mxfp4_launch_empty,
+    mxfp4_launch_minimal,
     mxfp4_measure_fp4_peak,
     mxfp4_prepack_b,
     mxfp4_prepack_b_bf16,
@@ -254,6 +255,15 @@ def launch_empty(count: int = 1, ctas: int = 32, device=None):
     torch = _torch()
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     _check(mxfp4_launch_empty(int(count), int(ctas), _stream_handle(dev)), "mxfp4_launch_empty")
+
+
+def launch_minimal(count: int = 1, ctas: int = 32, device=None):
+    """Enqueue `count` minimal kernels (a global read, a tensor-memory
+    allocation, a global write per CTA) on the current stream: the launch
+    floor of a tcgen05 GEMM."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _check(mxfp4_launch_minimal(int(count), int(ctas), _stream_handle(dev)), "mxfp4_launch_minimal")
 
 
 def gemm_noalloc(a, packed: PackedB, out=None):

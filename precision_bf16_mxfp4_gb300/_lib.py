@@ -27,7 +27,7 @@ EXPORTED = (
     "mxfp4_status_string", "mxfp4_version", "mxfp4_quant", "mxfp4_prepacked_b_bytes", "mxfp4_prepack_b",
     "mxfp4_gemm_workspace_bytes", "mxfp4_gemm", "mxfp4_gemm_noalloc", "mxfp4_device_status",
     "mxfp4_prepack_b_bf16", "mxfp4_act_image_bytes", "mxfp4_quant_image", "mxfp4_gemm_image",
-    "mxfp4_gemm_host", "mxfp4_measure_fp4_peak", "mxfp4_launch_empty", "mxfp4_set_debug_options",
+    "mxfp4_gemm_host", "mxfp4_measure_fp4_peak", "mxfp4_launch_empty", "mxfp4_launch_minimal", "mxfp4_set_debug_options",
     "mxfp4_kernel_binary_version",
 )
 
@@ -80,6 +80,8 @@ def load(build_if_missing: bool = True):
         lib.mxfp4_measure_fp4_peak.restype = i32
         lib.mxfp4_launch_empty.argtypes = [ctypes.c_int, ctypes.c_int, p]
         lib.mxfp4_launch_empty.restype = i32
+        lib.mxfp4_launch_minimal.argtypes = [ctypes.c_int, ctypes.c_int, p]
+        lib.mxfp4_launch_minimal.restype = i32
         lib.mxfp4_set_debug_options.argtypes = [i32, i32]
         lib.mxfp4_set_debug_options.restype = i32
         lib.mxfp4_kernel_binary_version.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -146,6 +148,10 @@ def mxfp4_measure_fp4_peak(kblocks_per_sm, tflops, stream) -> int:
 
 def mxfp4_launch_empty(count, ctas, stream) -> int:
     return int(load().mxfp4_launch_empty(count, ctas, stream))
+
+
+def mxfp4_launch_minimal(count, ctas, stream) -> int:
+    return int(load().mxfp4_launch_minimal(count, ctas, stream))
 
 
 def mxfp4_set_debug_options(split_k, drop_copies) -> int:

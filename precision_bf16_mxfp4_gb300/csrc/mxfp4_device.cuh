@@ -181,41 +181,71 @@ __device__ __forceinline__ int64_t div_seg(int64_t seg, int64_t d, bool small) {
 // stores fill one swizzled 128-byte row of a data tile and two lanes store
 // the row's scale words (blocks 0-3 and 4-7).  Segment s is row s / kt_count,
 // K block s % kt_count.  The calling warp takes segments lo + first,
-// lo + first + stride, ... below hi, loading kBatch of them before
-// quantizing any so that enough bytes are in flight to cover memory latency.
-// Rows >= m and K beyond k are written as zero codes with scale byte 0.
-// All 32 lanes must call it.
+// lo + first + stride, ... below hi, in batches of kBatch, software-pipelined:
+// the loads of the next batch are issued before the current batch is
+// quantized, so a warp's memory latency overlaps its own arithmetic.  Each
+// step moves the row and K block by the same amounts, so they are advanced
+// incrementally instead of divided out per segment.  Rows >= m and K beyond
+// k are written as zero codes with scale byte 0.  All 32 lanes must call it.
 template <bool kHw, int kBatch>
 __device__ __forceinline__ void quantize_image_segments(const uint16_t* __restrict__ a, int64_t m, int64_t k,
                                                         int64_t lda, uint8_t* __restrict__ img, int64_t kt_count,
                                                         int64_t lo, int64_t hi, int64_t first, int64_t stride,
                                                         int lane) {
-  const bool small = hi + stride * kBatch < (1ll << 31);
-  for (int64_t base = lo + first; base < hi; base += stride * kBatch) {
-    uint4 v[kBatch];
-    int64_t row[kBatch], kt[kBatch];
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      const int64_t seg = base + (int64_t)i * stride;
-      row[i] = div_seg(seg, kt_count, small);
-      kt[i] = seg - row[i] * kt_count;
-      const int64_t col = kt[i] * kTileK + lane * 8;
-      v[i] = (seg < hi && row[i] < m && col < k) ? ldg_nc_v4(a + row[i] * lda + col) : make_uint4(0, 0, 0, 0);
+  int64_t seg = lo + first;
+  if (seg >= hi) return;
+  int64_t row = seg / kt_count, kt = seg - row * kt_count;
+  const int64_t d_row = stride / kt_count, d_kt = stride - d_row * kt_count;
+  const int b = lane >> 2;
+  auto load = [&](int64_t r, int64_t t, bool ok) -> uint4 {
+    const int64_t col = t * kTileK + lane * 8;
+    return (ok && r < m && col < k) ? ldg_nc_v4(a + r * lda + col) : make_uint4(0, 0, 0, 0);
+  };
+  // the next segment of this warp: its row, K block, validity and bf16 data
+  auto take = [&](int64_t& r_out, int64_t& kt_out, bool& ok_out, uint4& v_out) {
+    r_out = row;
+    kt_out = kt;
+    ok_out = seg < hi;
+    v_out = load(row, kt, ok_out);
+    seg += stride;
+    row += d_row;
+    kt += d_kt;
+    if (kt >= kt_count) {
+      kt -= kt_count;
+      ++row;
     }
+  };
+  uint4 cur[kBatch];
+  int64_t crow[kBatch], ckt[kBatch];
+  bool cval[kBatch];
+#pragma unroll
+  for (int i = 0; i < kBatch; ++i) take(crow[i], ckt[i], cval[i], cur[i]);
+  while (cval[0]) {
+    uint4 nxt[kBatch];
+    int64_t nrow[kBatch], nkt[kBatch];
+    bool nval[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) take(nrow[i], nkt[i], nval[i], nxt[i]);
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
-      if (base + (int64_t)i * stride >= hi) break;  // uniform across the warp
+      if (!cval[i]) break;  // uniform across the warp
       uint32_t sbyte;
-      const uint32_t packed = quantize_quad<kHw>(v[i], sbyte);
-      const int r = (int)(row[i] & (kTileRows - 1));
-      const int b = lane >> 2;
-      uint8_t* tile = img + image_block(row[i] / kTileRows, kt[i], kt_count);
+      const uint32_t packed = quantize_quad<kHw>(cur[i], sbyte);
+      const int r = (int)(crow[i] & (kTileRows - 1));
+      uint8_t* tile = img + image_block(crow[i] / kTileRows, ckt[i], kt_count);
       *reinterpret_cast<uint32_t*>(tile + tile_data_offset(r, b * 16 + (lane & 3) * 4)) = packed;
       // scale word of blocks 0-3 (atom 0) and of blocks 4-7 (atom 1): byte b & 3
       uint32_t word = sbyte << (8 * (b & 3));
       word |= __shfl_xor_sync(0xFFFFFFFFu, word, 4);
       word |= __shfl_xor_sync(0xFFFFFFFFu, word, 8);
       if ((lane & 15) == 0) *reinterpret_cast<uint32_t*>(tile + kTileDataBytes + tile_sf_offset(r, b)) = word;
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      cur[i] = nxt[i];
+      crow[i] = nrow[i];
+      ckt[i] = nkt[i];
+      cval[i] = nval[i];
     }
   }
 }

@@ -6,7 +6,8 @@
 // per block, the GEMM kernels' own issue sequence) on operands that stay in
 // shared memory; nothing is loaded from or stored to global memory.  The
 // host times the launch with CUDA events and divides the FLOPs by it.  Also
-// the launch floor: empty kernels timed the way the GEMMs are.
+// the launch floors: empty kernels, and minimal kernels that touch global
+// and tensor memory, timed the way the GEMMs are.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -98,6 +99,25 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int64_t kbloc
 // An empty kernel: the launch floor that the small-m GEMM's time is read against.
 __global__ void empty_kernel() {}
 
+// The least a GEMM launch does: read a word of global memory, allocate and
+// free tensor memory, write a word.  After an L2 flush by writes, each of the
+// three alone already costs a kernel about 2 us of event time over the empty
+// one (measured on GB300), so this is the floor a tcgen05 GEMM meets.
+__device__ uint32_t g_minimal_words[4096 * 2];
+__global__ void minimal_kernel() {
+  __shared__ uint32_t slot;
+  const int i = blockIdx.x & 4095;
+  uint32_t v = 0;
+  if (threadIdx.x == 0) v = *reinterpret_cast<volatile uint32_t*>(&g_minimal_words[2 * i]);
+  tmem_alloc(&slot, 32);
+  tmem_relinquish();
+  tc_fence_before();
+  __syncwarp();
+  tc_fence_after();
+  tmem_dealloc(slot, 32);
+  if (threadIdx.x == 0) g_minimal_words[2 * i + 1] = v + 1;
+}
+
 }  // namespace
 }  // namespace mxfp4
 
@@ -105,6 +125,15 @@ extern "C" mxfp4_status mxfp4_launch_empty(int count, int ctas, void* stream) {
   if (count < 1 || count > 16 || ctas < 1 || ctas > 65535) return MXFP4_ERR_INVALID_ARG;
   for (int i = 0; i < count; ++i) {
     mxfp4::empty_kernel<<<ctas, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+    if (cudaGetLastError() != cudaSuccess) return MXFP4_ERR_CUDA;
+  }
+  return MXFP4_OK;
+}
+
+extern "C" mxfp4_status mxfp4_launch_minimal(int count, int ctas, void* stream) {
+  if (count < 1 || count > 16 || ctas < 1 || ctas > 65535) return MXFP4_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) {
+    mxfp4::minimal_kernel<<<ctas, 32, 0, static_cast<cudaStream_t>(stream)>>>();
     if (cudaGetLastError() != cudaSuccess) return MXFP4_ERR_CUDA;
   }
   return MXFP4_OK;

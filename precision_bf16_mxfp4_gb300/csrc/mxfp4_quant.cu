@@ -16,6 +16,7 @@ namespace mxfp4 {
 
 constexpr int kQuantThreads = 256;
 constexpr int kQuantSegBatch = 4;  // row segments whose loads one warp keeps in flight
+constexpr int kImageSegBatch = 2;  // the image writer's batch (two batches in registers)
 
 // Both quantizers work in row segments: 256 consecutive K elements (8 scale
 // blocks) of one row, one segment per warp.  Lane l holds elements 8l..8l+7
@@ -75,7 +76,7 @@ __global__ void __launch_bounds__(kQuantThreads)
   const int64_t kt_count = ceil_div(k, kTileK);
   const int64_t warps = (int64_t)gridDim.x * (kQuantThreads / 32);
   const int64_t w0 = (int64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
-  quantize_image_segments<kHw, kQuantSegBatch>(a, m, k, lda, img, kt_count, 0, rows_out * kt_count, w0, warps,
+  quantize_image_segments<kHw, kImageSegBatch>(a, m, k, lda, img, kt_count, 0, rows_out * kt_count, w0, warps,
                                                threadIdx.x & 31);
 }
 
@@ -125,16 +126,17 @@ static int grid_for(int64_t work_items, int per_block) {
   return (int)blocks;
 }
 
-// Grid of the quantization kernels: one warp per segment up to eight
-// 256-thread CTAs per SM (about two resident waves at these kernels'
-// register counts); beyond that each warp takes several segments, in
-// batches of kQuantSegBatch.  Measured on GB300 the image quantizer of a
-// 4096 x 2048 activation runs about 2 us above a plain copy of the same
-// input: its time goes to the dependent chains of the per-block arithmetic
-// as much as to HBM (a variant staging rows through shared memory with bulk
-// copies, eight warps per SM, was slower).
-static int quant_grid(int64_t segments) {
-  const int64_t max_warps = (int64_t)num_sms() * 8 * (kQuantThreads / 32);
+// Grid of the quantization kernels: one warp per segment, up to `per_sm`
+// 256-thread CTAs per SM; beyond that each warp takes several segments.
+// The weight quantizer runs up to eight CTAs per SM (about two resident
+// waves at its register count), loading kQuantSegBatch segments at a time.
+// The activation image writer runs one resident wave (four CTAs per SM at
+// its 64 registers) whose warps pipeline their segments: measured on GB300
+// at m = 4096, k = 2048 the quantizer alone takes the same time either way
+// (it reads A at what DRAM gives after an L2 flush by writes), but the
+// dependent GEMM's call finished 1.0 us sooner with the single wave.
+static int quant_grid(int64_t segments, int per_sm) {
+  const int64_t max_warps = (int64_t)num_sms() * per_sm * (kQuantThreads / 32);
   const int64_t warps = segments < max_warps ? segments : max_warps;
   const int64_t blocks = ceil_div(warps, (int64_t)(kQuantThreads / 32));
   return blocks < 1 ? 1 : (int)blocks;
@@ -142,7 +144,7 @@ static int quant_grid(int64_t segments) {
 
 cudaError_t launch_quant_linear(const void* a, int64_t m, int64_t k, int64_t lda, void* q, void* scale,
                                 cudaStream_t stream) {
-  const int grid = quant_grid(m * ceil_div(k, kTileK));
+  const int grid = quant_grid(m * ceil_div(k, kTileK), 8);
   quant_linear_kernel<kUseHardwareCvt><<<grid, kQuantThreads, 0, stream>>>(
       static_cast<const uint16_t*>(a), m, k, lda, static_cast<uint8_t*>(q), static_cast<uint8_t*>(scale));
   return cudaGetLastError();
@@ -151,7 +153,7 @@ cudaError_t launch_quant_linear(const void* a, int64_t m, int64_t k, int64_t lda
 cudaError_t launch_quant_image(const void* a, int64_t m, int64_t k, int64_t lda, void* img, cudaStream_t stream,
                                bool zero_padding_rows) {
   const int64_t rows_out = zero_padding_rows ? ceil_div(m, kTileRows) * kTileRows : m;
-  const int grid = quant_grid(rows_out * ceil_div(k, kTileK));
+  const int grid = quant_grid(rows_out * ceil_div(k, kTileK), 4);
   quant_image_kernel<kUseHardwareCvt><<<grid, kQuantThreads, 0, stream>>>(
       static_cast<const uint16_t*>(a), m, k, lda, static_cast<uint8_t*>(img), rows_out);
   return cudaGetLastError();

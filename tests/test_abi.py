@@ -187,6 +187,10 @@ def test_launch_empty_rejects_bad_arguments_without_a_gpu():
     assert mx.mxfp4_launch_empty(0, 32, None) == E
     assert mx.mxfp4_launch_empty(17, 32, None) == E
     assert mx.mxfp4_launch_empty(1, 0, None) == E
+    assert mx.mxfp4_launch_minimal(0, 32, None) == E
+    assert mx.mxfp4_launch_minimal(17, 32, None) == E
+    assert mx.mxfp4_launch_minimal(1, 0, None) == E
+    assert mx.mxfp4_launch_minimal(1, 65536, None) == E
 
 
 def test_product_path_does_not_touch_the_oracle():

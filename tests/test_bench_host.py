@@ -142,6 +142,12 @@ def test_shape_row_fraction_and_launch_floor_multiple():
     row2 = bench.shape_row(_W(64, 7168, 2048, "m64"), [14e-6], {1: 5.0, 2: 7.0}, 152)
     assert row2["launches"] == 2 and row2["launch_floor_us"] == 7.0 and row2["x_launch_floor"] == 2.0
     assert row2["kernels"] == "quant_image_kernel + gemm_kernel<64, image swap>"
+    assert "x_minimal_floor" not in row2
+    floors = {1: 5.0, 2: 7.0, ("minimal", 1): 6.0, ("minimal", 2): 8.0}
+    row3 = bench.shape_row(w, [12e-6], floors, 152)
+    assert row3["minimal_floor_us"] == 6.0 and row3["x_minimal_floor"] == 2.0 and row3["x_launch_floor"] == 2.4
+    row4 = bench.shape_row(_W(64, 7168, 2048, "m64"), [12e-6], floors, 152)
+    assert row4["minimal_floor_us"] == 8.0 and row4["x_minimal_floor"] == 1.5
 
 
 def test_roofline_picks_the_slowest_call_and_its_floor():

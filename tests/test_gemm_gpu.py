@@ -294,6 +294,10 @@ def test_fp4_peak_microbenchmark_is_plausible():
 
 def test_launch_floor_kernels_run():
     mx.launch_empty(2, 32)
+    # more CTAs than the SMs' tensor memory can hold at 32 columns each at
+    # once: allocations wait for other CTAs' frees, which always come
+    mx.launch_minimal(2, 32)
+    mx.launch_minimal(1, 4096)
     torch.cuda.synchronize()
     mx.device_status()
 
