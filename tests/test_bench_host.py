@@ -136,7 +136,8 @@ def test_shape_row_fraction_and_launch_floor_multiple():
     w = _W(32, 4096, 512, "m32_n4096_k512")
     row = bench.shape_row(w, [9e-6, 10e-6, 11e-6], {1: 5.0, 2: 7.0}, 152)
     hbm, _, _ = bench.load_peaks()
-    assert row["us_mean"] == 10.0 and row["us_median"] == 10.0
+    assert row["us_mean"] == 10.0 and row["us_median"] == 10.0 and row["us_trimmed"] == 10.0
+    assert bench.trimmed_mean([1.0, 5.0, 6.0, 7.0, 100.0]) == 6.0
     assert abs(row["frac"] - EXPECTED_BYTES[(32, 4096, 512)] / (hbm * 1e9) / 10e-6) < 1e-4
     assert row["launches"] == 1 and row["launch_floor_us"] == 5.0 and row["x_launch_floor"] == 2.0
     row2 = bench.shape_row(_W(64, 7168, 2048, "m64"), [14e-6], {1: 5.0, 2: 7.0}, 152)
