@@ -20,6 +20,10 @@ bool valid_k(int64_t k) { return k > 0 && (k % 32) == 0; }
 // The address through which kernels reach page-locked host memory (mapped
 // into every device's address space under unified addressing), else nullptr
 // (pageable memory, or a pointer the runtime does not know).
+// Largest k for which mxfp4_gemm_host lets the fused kernel work on host
+// memory directly.
+constexpr int64_t kDirectHostMaxK = 512;
+
 void* mapped_host(const void* p) {
   cudaPointerAttributes at{};
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
@@ -106,10 +110,14 @@ mxfp4_status mxfp4_gemm_host(const void* a_host, int64_t m, int64_t k, int64_t l
   if (mxfp4::make_gemm_plan(m, n, k, &plan) != 0) return MXFP4_ERR_UNSUPPORTED;
   if (plan.workspace > 0 && (!workspace || workspace_bytes < plan.workspace)) return MXFP4_ERR_WORKSPACE;
   if (plan.workspace > 0 && !aligned16(workspace)) return MXFP4_ERR_INVALID_ARG;
-  if (plan.mode == 0) {
+  if (plan.mode == 0 && k <= kDirectHostMaxK) {
     // The fused small-m kernel reads A with plain loads and writes C with
     // plain stores, so with page-locked buffers it works on host memory
-    // directly (NVLink-C2C on GB300): no copy on either side.
+    // directly (NVLink-C2C on GB300): no copy on either side.  Only while a
+    // CTA's whole K range of A goes out in one round of loads: each further
+    // round waits a host-memory round trip (m = 16, k = 7168 measured 48 us
+    // this way against 28 us with the two copies; m = 32, k = 512 10-20 us,
+    // as fast as or faster than the copies).
     const void* a_map = mapped_host(a_host);
     void* c_map = a_map ? mapped_host(c_host) : nullptr;
     if (a_map && c_map && aligned16(a_map) && aligned16(c_map) && (lda % 8) == 0 && (ldc % 8) == 0)

@@ -178,7 +178,7 @@ def test_gemm_ragged_shapes_with_padded_strides(m, n, k):
     assert torch.isnan(c_full[:, n:]).all(), "wrote outside the [m, n] window"
 
 
-HOST_CASES = [(32, 2880, 512), (4, 129, 288), (17, 136, 1024), (200, 1003, 544), (1024, 4864, 256)]
+HOST_CASES = [(32, 2880, 512), (4, 129, 288), (17, 136, 1024), (16, 640, 7168), (200, 1003, 544), (1024, 4864, 256)]
 
 
 @pytest.mark.parametrize("m,n,k", HOST_CASES)
