@@ -32,7 +32,9 @@
  *     kernel attributes and occupancy figures, and the watchdog flag of
  *     mxfp4_device_status (a device variable every kernel of the library
  *     may set); per host thread, the last few tensor maps of C the
- *     large-m GEMM was launched with; per process, the overrides of
+ *     large-m GEMM was launched with, and per host thread and device the
+ *     helper stream and five events of mxfp4_gemm_host's chunked round trip
+ *     (created on first use, never destroyed); per process, the overrides of
  *     mxfp4_set_debug_options.  The exception is mxfp4_gemm_noalloc: its
  *     scratch is one device array shared by every call on a device, so
  *     calls of it that overlap on the GPU race (see its declaration).
@@ -163,7 +165,15 @@ MXFP4_API mxfp4_status mxfp4_gemm(const void* a_bf16, int64_t m, int64_t k, int6
  * that is wanted there: on `stream`, one 2-D copy of A to the device, the
  * GEMM of mxfp4_gemm, one 2-D copy of C back.  The pages' entry point takes
  * its input tuple and returns C (submission 752099, `custom_kernel`); this is
- * that round trip for a caller whose tensors are in host memory.
+ * that round trip for a caller whose tensors are in host memory.  When C is
+ * at least 8 MiB (m > 32, m >= 512) the round trip runs in up to four chunks
+ * of whole 256-row tiles: each chunk's A copy and GEMM on `stream`, its C
+ * copy on a helper stream of the library after that GEMM, so that the
+ * downloads overlap the later chunks; `stream` then waits for the last
+ * download, so work enqueued on it after the call sees the whole C.  During
+ * stream capture the chunked form is used only if the helper stream already
+ * exists (an earlier call on this host thread and device created it);
+ * otherwise the call takes the single-stream form.
  *   a_host   : bf16 [m, k] in host memory, row stride lda elements
  *   b_packed : image from mxfp4_prepack_b for (n, k), in device memory
  *   c_host   : bf16 [m, n] in host memory, row stride ldc elements (written)

@@ -1,6 +1,7 @@
 // C ABI of the MXFP4 library: argument validation, then kernel launches on
 // the caller's stream.  Nothing here allocates device memory or blocks,
-// except mxfp4_device_status.
+// except mxfp4_device_status; mxfp4_gemm_host keeps one helper stream and a
+// few events per host thread and device for its chunked round trip.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -23,6 +24,52 @@ bool valid_k(int64_t k) { return k > 0 && (k % 32) == 0; }
 // Largest k for which mxfp4_gemm_host lets the fused kernel work on host
 // memory directly.
 constexpr int64_t kDirectHostMaxK = 512;
+
+// Round trips whose C is at least kChunkMinCBytes split m into up to
+// kMaxChunks row chunks of whole 256-row tiles: each chunk's C goes down on a
+// helper stream while the next chunk's A goes up and its GEMM runs on the
+// caller's stream.  The host link carries both directions at once (on GB300
+// ~190-205 GB/s each way; a 58.7 MB download took 311 us alone and 327 us
+// beside an upload), so at m = 4096, n = 7168 the downloads of the first
+// chunks hide the rest of the work: 437 us in one stream, 378 us in four
+// chunks, 409 us in eight (more, smaller GEMMs and copies).
+constexpr size_t kChunkMinCBytes = size_t(8) << 20;
+constexpr int kMaxChunks = 4;
+constexpr int64_t kChunkRowAlign = 256;
+
+// The helper stream and events of the calling host thread on the current
+// device, created on first use and kept for the life of the thread (they
+// are never destroyed); nullptr if they do not exist and may not be created
+// now (during stream capture), or if creating them failed, in which case
+// the caller takes the single-stream path.
+struct HostPipe {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t ev[kMaxChunks + 1] = {};
+  bool ready = false;
+  bool failed = false;
+};
+
+HostPipe* host_pipe(bool may_create) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  thread_local HostPipe pipes[64];
+  HostPipe& p = pipes[dev];
+  if (p.ready) return &p;
+  if (p.failed || !may_create) return nullptr;
+  bool ok = cudaStreamCreateWithFlags(&p.stream, cudaStreamNonBlocking) == cudaSuccess;
+  for (int i = 0; ok && i <= kMaxChunks; ++i)
+    ok = cudaEventCreateWithFlags(&p.ev[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    (void)cudaGetLastError();
+    p.failed = true;
+    return nullptr;
+  }
+  p.ready = true;
+  return &p;
+}
 
 void* mapped_host(const void* p) {
   cudaPointerAttributes at{};
@@ -123,11 +170,43 @@ mxfp4_status mxfp4_gemm_host(const void* a_host, int64_t m, int64_t k, int64_t l
     if (a_map && c_map && aligned16(a_map) && aligned16(c_map) && (lda % 8) == 0 && (ldc % 8) == 0)
       return mxfp4_gemm(a_map, m, k, lda, b_packed, n, c_map, ldc, workspace, workspace_bytes, stream);
   }
-  if (cudaMemcpy2DAsync(a_dev, k * esz, a_host, lda * esz, k * esz, m, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return MXFP4_ERR_CUDA;
-  const mxfp4_status s = mxfp4_gemm(a_dev, m, k, k, b_packed, n, c_dev, n8, workspace, workspace_bytes, stream);
-  if (s != MXFP4_OK) return s;
-  return from_cuda(cudaMemcpy2DAsync(c_host, ldc * esz, c_dev, n8 * esz, n * esz, m, cudaMemcpyDeviceToHost, st));
+  const auto* ah = static_cast<const uint8_t*>(a_host);
+  auto* ch = static_cast<uint8_t*>(c_host);
+  auto* ad = static_cast<uint8_t*>(a_dev);
+  auto* cd = static_cast<uint8_t*>(c_dev);
+  HostPipe* hp = nullptr;
+  if (m > 32 && static_cast<size_t>(m) * static_cast<size_t>(n) * esz >= kChunkMinCBytes && m >= 2 * kChunkRowAlign) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MXFP4_ERR_CUDA;
+    hp = host_pipe(cap == cudaStreamCaptureStatusNone);
+  }
+  if (!hp) {
+    if (cudaMemcpy2DAsync(a_dev, k * esz, a_host, lda * esz, k * esz, m, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return MXFP4_ERR_CUDA;
+    const mxfp4_status s = mxfp4_gemm(a_dev, m, k, k, b_packed, n, c_dev, n8, workspace, workspace_bytes, stream);
+    if (s != MXFP4_OK) return s;
+    return from_cuda(cudaMemcpy2DAsync(c_host, ldc * esz, c_dev, n8 * esz, n * esz, m, cudaMemcpyDeviceToHost, st));
+  }
+  // chunked: up, GEMM, (fork) down, per chunk of rows; the caller's stream
+  // waits for the last download before anything enqueued after this call
+  int64_t rows = (m + kMaxChunks - 1) / kMaxChunks;
+  rows = (rows + kChunkRowAlign - 1) / kChunkRowAlign * kChunkRowAlign;
+  int i = 0;
+  for (int64_t r0 = 0; r0 < m; r0 += rows, ++i) {
+    const int64_t mr = m - r0 < rows ? m - r0 : rows;
+    if (cudaMemcpy2DAsync(ad + r0 * k * esz, k * esz, ah + r0 * lda * esz, lda * esz, k * esz, mr,
+                          cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return MXFP4_ERR_CUDA;
+    const mxfp4_status s = mxfp4_gemm(ad + r0 * k * esz, mr, k, k, b_packed, n, cd + r0 * n8 * esz, n8, workspace,
+                                      workspace_bytes, stream);
+    if (s != MXFP4_OK) return s;
+    if (cudaEventRecord(hp->ev[i], st) != cudaSuccess || cudaStreamWaitEvent(hp->stream, hp->ev[i], 0) != cudaSuccess ||
+        cudaMemcpy2DAsync(ch + r0 * ldc * esz, ldc * esz, cd + r0 * n8 * esz, n8 * esz, n * esz, mr,
+                          cudaMemcpyDeviceToHost, hp->stream) != cudaSuccess)
+      return MXFP4_ERR_CUDA;
+  }
+  if (cudaEventRecord(hp->ev[kMaxChunks], hp->stream) != cudaSuccess) return MXFP4_ERR_CUDA;
+  return from_cuda(cudaStreamWaitEvent(st, hp->ev[kMaxChunks], 0));
 }
 
 mxfp4_status mxfp4_prepack_b_bf16(const void* b_bf16, int64_t n, int64_t k, int64_t ldb, void* b_packed,

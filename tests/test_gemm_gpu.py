@@ -178,7 +178,10 @@ def test_gemm_ragged_shapes_with_padded_strides(m, n, k):
     assert torch.isnan(c_full[:, n:]).all(), "wrote outside the [m, n] window"
 
 
-HOST_CASES = [(32, 2880, 512), (4, 129, 288), (17, 136, 1024), (16, 640, 7168), (200, 1003, 544), (1024, 4864, 256)]
+# the last two have a C of at least 8 MiB: the chunked round trip (4 chunks
+# of 256 rows; 512, 512 and a ragged 76)
+HOST_CASES = [(32, 2880, 512), (4, 129, 288), (17, 136, 1024), (16, 640, 7168), (200, 1003, 544), (1024, 4864, 256),
+              (1100, 4856, 512)]
 
 
 @pytest.mark.parametrize("m,n,k", HOST_CASES)
@@ -223,6 +226,35 @@ def test_gemm_host_reuses_its_buffers_across_calls():
         torch.cuda.synchronize()
         want = mx.gemm(a.cuda(), packed).cpu()
         assert torch.equal(c_host.view(torch.int16), want.view(torch.int16))
+
+
+def test_gemm_host_chunked_round_trip_in_a_captured_cuda_graph():
+    # the chunked form forks its downloads onto the library's helper stream
+    # and joins them back; captured (after an uncaptured call made the helper
+    # stream) and replayed with new A, it must give the device call's C
+    m, n, k = 1024, 4864, 512
+    packed, _, _ = packed_from_oracle(inputs.random_bf16(n, k, seed=7))
+    a_host = inputs.random_bf16(m, k, seed=8).pin_memory()
+    c_host = torch.empty((m, n), dtype=torch.bfloat16).pin_memory()
+    a_dev = torch.empty((m, k), dtype=torch.bfloat16, device="cuda")
+    c_dev = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(mx.workspace_bytes(m, n, k), 16), dtype=torch.uint8, device="cuda")
+    call = lambda: mx.gemm_host(a_host, packed, out=c_host, a_dev=a_dev, c_dev=c_dev, workspace=ws)
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    torch.cuda.synchronize()
+    for seed in (9, 10):
+        a = inputs.random_bf16(m, k, seed=seed)
+        a_host.copy_(a)
+        c_host.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        want = mx.gemm(a.cuda(), packed).cpu()
+        assert torch.equal(c_host.view(torch.int16), want.view(torch.int16))
+    mx.device_status()
 
 
 def test_gemm_deterministic_and_reusable_workspace():
