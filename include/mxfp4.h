@@ -183,11 +183,13 @@ MXFP4_API mxfp4_status mxfp4_gemm(const void* a_bf16, int64_t m, int64_t k, int6
  *   workspace: as mxfp4_gemm
  * With page-locked host buffers the call only enqueues; C is complete in
  * c_host once `stream` has passed the call (synchronize before reading it).
- * For m <= 32 and k <= 512 with page-locked buffers whose row strides are
- * multiples of 8 elements (16-byte aligned rows), the fused kernel reads A
- * from and writes C to host memory directly (mapped into the device's address
- * space; over NVLink-C2C on GB300) and the staging buffers are not touched;
- * otherwise the two copies go through a_dev and c_dev.  With pageable host buffers the
+ * With page-locked buffers whose row strides are multiples of 8 elements
+ * (16-byte aligned rows), the kernels read A from and write C to host memory
+ * directly (mapped into the device's address space; over NVLink-C2C on
+ * GB300) and the staging buffers are not touched, except for the large-m
+ * CTA-pair plan (C stored by tensor-map bulk copies) and for m <= 32 with
+ * k > 512 (A read in several rounds of host round trips); those take the two
+ * copies through a_dev and c_dev.  With pageable host buffers the
  * runtime stages the copies and the call may block.  The caller owns every
  * buffer; nothing is allocated.
  * Preconditions: m, n > 0, k > 0, k % 32 == 0, lda >= k, ldc >= n, host

@@ -157,14 +157,18 @@ mxfp4_status mxfp4_gemm_host(const void* a_host, int64_t m, int64_t k, int64_t l
   if (mxfp4::make_gemm_plan(m, n, k, &plan) != 0) return MXFP4_ERR_UNSUPPORTED;
   if (plan.workspace > 0 && (!workspace || workspace_bytes < plan.workspace)) return MXFP4_ERR_WORKSPACE;
   if (plan.workspace > 0 && !aligned16(workspace)) return MXFP4_ERR_INVALID_ARG;
-  if (plan.mode == 0 && k <= kDirectHostMaxK) {
-    // The fused small-m kernel reads A with plain loads and writes C with
-    // plain stores, so with page-locked buffers it works on host memory
-    // directly (NVLink-C2C on GB300): no copy on either side.  Only while a
-    // CTA's whole K range of A goes out in one round of loads: each further
-    // round waits a host-memory round trip (m = 16, k = 7168 measured 48 us
-    // this way against 28 us with the two copies; m = 32, k = 512 10-20 us,
-    // as fast as or faster than the copies).
+  // The fused small-m kernel, the activation quantizer and the one-CTA
+  // GEMMs read A with plain loads and write C with plain stores, so with
+  // page-locked buffers they work on host memory directly (NVLink-C2C on
+  // GB300): no copy on either side.  Not the CTA-pair plan, whose C goes out
+  // through tensor-map bulk stores, and not the fused kernel beyond one
+  // round of A loads per CTA: each further round waits a host-memory round
+  // trip (m = 16, k = 7168 measured 48 us this way against 27 us with the
+  // two copies; m = 32, k = 512 10-20 us, as fast as or faster than the
+  // copies; m = 64, k = 2048 17 us against 36 us; m = 256, k = 1536 23 us
+  // against 38 us).
+  const bool direct = plan.mode == 0 ? k <= kDirectHostMaxK : !plan.persistent;
+  if (direct) {
     const void* a_map = mapped_host(a_host);
     void* c_map = a_map ? mapped_host(c_host) : nullptr;
     if (a_map && c_map && aligned16(a_map) && aligned16(c_map) && (lda % 8) == 0 && (ldc % 8) == 0)

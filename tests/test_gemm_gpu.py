@@ -180,8 +180,8 @@ def test_gemm_ragged_shapes_with_padded_strides(m, n, k):
 
 # the last two have a C of at least 8 MiB: the chunked round trip (4 chunks
 # of 256 rows; 512, 512 and a ragged 76)
-HOST_CASES = [(32, 2880, 512), (4, 129, 288), (17, 136, 1024), (16, 640, 7168), (200, 1003, 544), (1024, 4864, 256),
-              (1100, 4856, 512)]
+HOST_CASES = [(32, 2880, 512), (4, 129, 288), (17, 136, 1024), (16, 640, 7168), (64, 2000, 2048), (200, 1003, 544),
+              (1024, 4864, 256), (1100, 4856, 512)]
 
 
 @pytest.mark.parametrize("m,n,k", HOST_CASES)
@@ -189,9 +189,10 @@ HOST_CASES = [(32, 2880, 512), (4, 129, 288), (17, 136, 1024), (16, 640, 7168), 
 def test_gemm_host_round_trip(m, n, k, layout):
     # C lands in a wider NaN-filled host buffer, equal bit for bit to the
     # device call, with nothing outside the [m, n] window written.  Aligned
-    # page-locked rows let the small-m plan work on host memory directly;
-    # row strides that are not multiples of 8 elements, or pageable memory,
-    # take the copies through the device staging buffers.
+    # page-locked rows let every plan but the CTA-pair one and the fused one
+    # at k > 512 work on host memory directly; row strides that are not
+    # multiples of 8 elements, or pageable memory, take the copies through
+    # the device staging buffers.
     a = inputs.random_bf16(m, k, seed=m + 3 * n + 5 * k)
     b = inputs.random_bf16(n, k, seed=n + k, std=0.5)
     packed, bq, bs = packed_from_oracle(b)
