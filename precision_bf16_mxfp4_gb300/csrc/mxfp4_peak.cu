@@ -1,5 +1,5 @@
 // Dense FP4 tensor-core rate of this GPU: the denominator of the large-m
-// GEMM's roofline fraction (the measured peaks the pool provides cover HBM
+// GEMM's roofline fraction (the measured peak figures at hand cover HBM
 // and bf16 only).  One CTA per SM keeps a 128 x 256 fp32 accumulator in
 // tensor memory and one thread issues back-to-back 128 x 256 x 256
 // block-scaled K blocks (tcgen05.mma kind::mxf4, eight MMAs of 128 x 128 x 64
