@@ -178,6 +178,64 @@ def test_gemm_ragged_shapes_with_padded_strides(m, n, k):
     assert torch.isnan(c_full[:, n:]).all(), "wrote outside the [m, n] window"
 
 
+def _random_shapes(count=40, seed=20261202, budget=3e9):
+    """A fixed, seeded spread of (m, n, k) over every plan of the library:
+    fused (m <= 32, with and without a K split), image swap (m <= 128),
+    image plain and the CTA-pair kernel (many 256 x 256 tiles), each with an
+    oracle cost below `budget` multiply-adds."""
+    rng = np.random.default_rng(seed)
+    out = []
+    bands = [(1, 32), (33, 128), (129, 640), (641, 2200)]
+    while len(out) < count:
+        band = len(out) % len(bands)
+        lo, hi = bands[band]
+        m = int(rng.integers(lo, hi + 1))
+        if band == 3:  # enough 256 x 256 tiles for the CTA-pair plan
+            n_min = -(-152 // -(-m // 256)) * 256 - 255
+            n = int(rng.integers(n_min, n_min + 2000))
+        else:
+            n = int(rng.integers(1, 5200))
+        k_max = min(120, int(budget // (m * n * 32)))
+        if k_max < 1:
+            continue
+        out.append((m, n, 32 * int(rng.integers(1, k_max + 1))))
+    return out
+
+
+RANDOM_SHAPES = _random_shapes()
+
+
+@pytest.mark.parametrize("m,n,k", RANDOM_SHAPES)
+def test_gemm_random_shapes_sweep(m, n, k):
+    # a seeded sweep of shapes with odd sizes everywhere, padded strides and a
+    # NaN-poisoned C: every plan the library has, against the fp64 oracle
+    a = inputs.random_bf16(m, k, seed=m + 31 * n + 7 * k)
+    b = inputs.random_bf16(n, k, seed=3 * m + n + k, std=0.3)
+    packed, bq, bs = packed_from_oracle(b)
+    lda = k + 8 * (n % 3)
+    ldc = n + (8 - n % 8) % 8 + 8 * (m % 2)
+    got, c_full = _run(a, packed, lda=lda, ldc=ldc)
+    assert_close_to_ref(got, _oracle_full(a, bq, bs), what=f"{m}x{n}x{k}")
+    if ldc > n:
+        assert torch.isnan(c_full[:, n:]).all(), "wrote outside the [m, n] window"
+
+
+def test_random_shapes_cover_every_plan():
+    # the sweep above reaches the fused, split, image and CTA-pair plans
+    sms = 152
+    kinds = set()
+    for m, n, k in RANDOM_SHAPES:
+        if m <= 32:
+            kinds.add("fused")
+        elif m <= 128:
+            kinds.add("image swap")
+        elif n >= 256 and -(-m // 128) * -(-n // 256) >= sms:
+            kinds.add("pair")
+        else:
+            kinds.add("image plain")
+    assert kinds == {"fused", "image swap", "image plain", "pair"}, kinds
+
+
 # the last two have a C of at least 8 MiB: the chunked round trip (4 chunks
 # of 256 rows; 512, 512 and a ragged 76)
 HOST_CASES = [(32, 2880, 512), (4, 129, 288), (17, 136, 1024), (16, 640, 7168), (64, 2000, 2048), (200, 1003, 544),
