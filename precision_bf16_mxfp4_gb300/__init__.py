@@ -202,11 +202,14 @@ def gemm(a, packed: PackedB, out=None, workspace=None):
 
 def gemm_host(a_host, packed: PackedB, out=None, a_dev=None, c_dev=None, workspace=None):
     """C = quant(a_host) . B^T for a host-memory A, into host memory, through
-    mxfp4_gemm_host: A's upload, the GEMM and C's download are enqueued on the
-    current stream of B's device.  `out` (bf16 [m, n], host) is created
-    page-locked when not given; the device staging buffers and the workspace
-    are allocated when not given.  The result is in `out` once the stream has
-    reached the download (synchronize before reading it)."""
+    mxfp4_gemm_host, on the current stream of B's device.  With page-locked
+    buffers the kernels work on host memory directly, except for the large-m
+    CTA-pair plan and the fused plan at k > 512, which copy A up and C down
+    through the device staging buffers (in row chunks whose downloads
+    overlap the later chunks when C is 8 MiB or more).  `out` (bf16 [m, n],
+    host) is created page-locked when not given; the staging buffers and the
+    workspace are allocated when not given.  The result is in `out` once the
+    stream has passed the call (synchronize before reading it)."""
     torch = _torch()
     if a_host.is_cuda:
         raise ValueError("a_host must be a host tensor (use gemm for device tensors)")
