@@ -78,6 +78,50 @@ def test_gemm_large_workload_full_output():
     np.testing.assert_allclose(oracle.gemm_entries(aq, a_s, bq, bs, rows, cols), ref[rows, cols], rtol=1e-12)
 
 
+LARGEST = [
+    (32768, 7168, 2048),  # CTA-pair kernel, 3584 tiles: 47 rounds per pair
+    (2048, 4096, 16384),  # CTA-pair kernel, 32 stages per tile
+    (8, 2112, 65536),     # fused kernel, K split over 8-CTA clusters, 32 K blocks per rank
+    (8, 7168, 65536),     # fused kernel, 2 ranks (56 column tiles fill the SMs), 128 K blocks per rank
+    (64, 65536, 2048),    # quantizer + image swap-AB, 512 CTAs in several waves
+    (32, 65536, 512),     # fused kernel unsplit, 512 CTAs in several waves
+    (256, 1024, 32768),   # quantizer + image plain, K split over 8-CTA clusters
+]
+
+
+@pytest.mark.parametrize("m,n,k", LARGEST)
+def test_gemm_largest_shapes_sampled(m, n, k):
+    """Shapes far beyond the benchmark's, on every plan: C poisoned with NaN
+    must come back finite everywhere, and sampled entries (the last whole
+    column, 2000 random positions, and the first and last whole rows where
+    the oracle's budget of ~1.5e8 multiply-adds allows) must match the
+    oracle.  B is a random valid MXFP4 matrix (every e2m1 code, scales
+    2^-9..2^9): quantizing a bf16 B of this size in the oracle would take
+    minutes."""
+    rng = np.random.default_rng(m * 131 + n * 7 + k)
+    bq = rng.integers(0, 256, (n, k // 2), dtype=np.uint8)
+    bs = rng.integers(118, 137, (n, k // 32), dtype=np.uint8)
+    packed = mx.prepack_b(torch.from_numpy(bq).cuda(), torch.from_numpy(bs).cuda())
+    a = inputs.random_bf16(m, k, seed=m + n + k)
+    c = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mx.gemm(a.cuda(), packed, out=c)
+    mx.device_status()
+    assert not torch.isnan(c).any().item(), "entries of C were not written"
+    rows = [np.arange(m, dtype=np.int64), rng.integers(0, m, 2000)]
+    cols = [np.full(m, n - 1, np.int64), rng.integers(0, n, 2000)]
+    budget = int(1.5e8 // k) - m - 2000
+    for r in (0, m - 1):
+        if budget >= n:
+            rows.append(np.full(n, r, np.int64))
+            cols.append(np.arange(n, dtype=np.int64))
+            budget -= n
+    rows, cols = np.concatenate(rows), np.concatenate(cols)
+    got = c[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].float().cpu().numpy()
+    aq, a_s = oracle.quant(bf16_bits(a))
+    ref = oracle.gemm_entries(aq, a_s, bq, bs, rows, cols)
+    assert_close_to_ref(got, ref, what=f"{m}x{n}x{k}")
+
+
 def _selection_weights(n, k, cols):
     """MXFP4 weights whose row j is 1.0 at K column cols[j] (no entry where
     cols[j] < 0) and zero elsewhere, every scale 2^0: row j of B^T picks
