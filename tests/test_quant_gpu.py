@@ -130,6 +130,14 @@ def test_quant_ragged_shapes(m, k, lda):
     _check(a, lda=lda)
 
 
+@pytest.mark.parametrize("m,k,lda", [(32768, 4096, 4096), (3, 262144, 262144), (65536, 64, 72)])
+def test_quant_largest_shapes(m, k, lda):
+    # far beyond the workloads: 134 M elements; rows of 8192 blocks; 65536
+    # rows of two blocks with a padded stride - every byte against the oracle
+    a = inputs.random_bf16(m, k, seed=m + k, std=3.0)
+    _check(a, lda=lda)
+
+
 def test_quant_empty_is_a_noop():
     a = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
     q, s = mx.quant(a)
