@@ -25,7 +25,7 @@
  *   - Element strides (lda, ldc) are in elements, row-major.
  *   - Errors: MXFP4_ERR_INVALID_ARG / MXFP4_ERR_UNSUPPORTED are returned
  *     before anything is enqueued; MXFP4_ERR_CUDA reports a launch failure
- *     (cudaGetLastError right after the launch); faults that happen later
+ *     (the error status of the launch itself); faults that happen later
  *     surface at the caller's next synchronization, as with any CUDA call.
  *   - Entry points may be called from several host threads and on several
  *     streams at once.  The state the library keeps: per device, cached
