@@ -308,9 +308,9 @@ MXFP4_API mxfp4_status mxfp4_launch_empty(int count, int ctas, void* stream);
  * (1..65535) 32-thread CTAs on `stream`: each CTA reads one word of a
  * library-owned device array, allocates and frees 32 tensor-memory columns
  * and writes one word of the same array.  That is the least any GEMM launch
- * does, and after an L2 flush by writes each of the three costs a kernel
- * about as much event time as the empty kernel's whole launch overhead, so
- * this is the floor a tcgen05 GEMM can meet.  Overlapping calls race on the
+ * does; after an L2 flush by writes, any one of the three adds about 2 us
+ * of event time to an empty kernel on GB300 (all three together the same),
+ * so this is the floor a tcgen05 GEMM can meet.  Overlapping calls race on the
  * array, harmlessly (its values are never read by anything else).
  * Errors: MXFP4_ERR_INVALID_ARG, MXFP4_ERR_CUDA.
  */
